@@ -1,0 +1,91 @@
+"""The CPU oracle against what the pages and the mathematics fix (no GPU).
+
+Every pin in tests/pins.py runs against the oracle as built.  The mutation
+tests then compile copies of oracle.c with one plausible mistake planted each
+(a dropped term, a wrong index, a flipped sign, a reversed order, a wrong
+bias...) and check that some pin fails for every one of them.
+"""
+import os
+import subprocess
+import tempfile
+
+import pytest
+
+import oracle
+from tests import pins
+
+
+@pytest.mark.parametrize("pin", pins.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(pin, olib):
+    pin(olib)
+
+
+# (name, exact text in oracle.c, replacement, pins expected to catch it)
+MUTANTS = [
+    ("plan_cursor_not_advanced", "cursor[e] += 1;", ";",
+     [pins.pin_plan_hand_example, pins.pin_plan_bruteforce]),
+    ("plan_scan_inclusive", "off[e + 1] = off[e] + cnt[e];", "off[e + 1] = off[e] + cnt[e] + (e == 0);",
+     [pins.pin_plan_hand_example, pins.pin_plan_bruteforce]),
+    ("plan_accepts_E", "if (e >= 0 && e < E) {\n                int64_t row",
+     "if (e >= 0 && e <= E) {\n                int64_t row", [pins.pin_plan_bruteforce]),
+    ("plan_reverse_tokens", "for (int64_t s = 0; s < S; ++s) {\n        for (int k = 0; k < K; ++k) {\n            int64_t i = s * K + k;\n            int32_t e",
+     "for (int64_t s = S - 1; s >= 0; --s) {\n        for (int k = 0; k < K; ++k) {\n            int64_t i = s * K + k;\n            int32_t e",
+     [pins.pin_plan_hand_example, pins.pin_plan_bruteforce]),
+    ("plan_src_is_token", "packed_src[row] = (int32_t)i;", "packed_src[row] = (int32_t)s;",
+     [pins.pin_plan_hand_example, pins.pin_plan_bruteforce]),
+    ("group_rep_last_not_first", "if (group_of(topk_idx[s * K + kp], E, group_size) == g)\n                    first = 0;",
+     "if (group_of(topk_idx[s * K + kp], E, group_size) == g && 0)\n                    first = 0;",
+     [pins.pin_group_plan_bruteforce, pins.pin_group_plan_invariants]),
+    ("group_map_wrong_token", "grp_tok_map[r * K + k2] = (g2 == g) ? tok_map[s * K + k2] : -1;",
+     "grp_tok_map[r * K + k2] = (g2 == g) ? tok_map[s * K + k] : -1;",
+     [pins.pin_group_plan_bruteforce, pins.pin_dispatch_dedup]),
+    ("dispatch_wrong_source_row", "memcpy(packed + row * row_bytes, rows + s * row_bytes",
+     "memcpy(packed + row * row_bytes, rows + (s ^ 1) * row_bytes",
+     [pins.pin_dispatch_scatter, pins.pin_combine_identity_telescopes]),
+    ("combine_drops_last_k", "for (int k = 0; k < K; ++k) {\n                int64_t row = tok_map[s * K + k];",
+     "for (int k = 0; k < K - 1; ++k) {\n                int64_t row = tok_map[s * K + k];",
+     [pins.pin_combine_identity_telescopes, pins.pin_combine_exact_rational]),
+    ("combine_reverse_k", "for (int k = 0; k < K; ++k) {\n                int64_t row = tok_map[s * K + k];",
+     "for (int k = K - 1; k >= 0; --k) {\n                int64_t row = tok_map[s * K + k];",
+     [pins.pin_combine_k_order]),
+    ("combine_weight_index", "float term = w[s * K + k] * load_elem(y, in_dt, row * H + j);\n                acc = acc + term;\n            }\n            store_elem(out",
+     "float term = w[k] * load_elem(y, in_dt, row * H + j);\n                acc = acc + term;\n            }\n            store_elem(out",
+     [pins.pin_combine_identity_telescopes, pins.pin_combine_exact_rational]),
+    ("combine_sign", "acc = acc + term;\n            }\n            store_elem(out",
+     "acc = acc - term;\n            }\n            store_elem(out",
+     [pins.pin_combine_identity_telescopes]),
+    ("combine_transposed_y", "load_elem(y, in_dt, row * H + j);\n                acc = acc + term;\n            }\n            store_elem(out",
+     "load_elem(y, in_dt, j * H + row);\n                acc = acc + term;\n            }\n            store_elem(out",
+     [pins.pin_combine_identity_telescopes, pins.pin_combine_exact_rational]),
+    ("dedup_stage2_weighted", "acc = acc + gtok[r * H + j];", "acc = acc + w[s * K + k] * gtok[r * H + j];",
+     [pins.pin_combine_dedup_closed_forms]),
+    ("bf16_ties_away", "if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u)))",
+     "if (rest >= 0x8000u)", [pins.pin_bf16_rounding]),
+    ("bf16_truncates", "keep += 1u;", ";", [pins.pin_bf16_rounding, pins.pin_combine_exact_rational]),
+    ("e4m3_bias_8", "pow(2.0, ex - 7)", "pow(2.0, ex - 8)", [pins.pin_e4m3_table]),
+    ("e4m3_subnormal_exp", "pow(2.0, -6)", "pow(2.0, -7)", [pins.pin_e4m3_table]),
+    ("expert_scale_wrong_expert", "* c[e]);", "* c[e == 0 ? 0 : e - 1]);",
+     [pins.pin_expert_stages, pins.pin_combine_expert_scale_closed_form]),
+    ("dequant_wrong_block", "scales[r * nb + j / block]", "scales[r * nb + j % nb]",
+     [pins.pin_expert_stages]),
+]
+
+
+@pytest.mark.parametrize("name,old,new,catchers", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, old, new, catchers, tmp_path):
+    src = open(oracle._SRC).read()
+    assert src.count(old) >= 1, f"anchor for mutant {name} not found in oracle.c"
+    mutated = src.replace(old, new, 1)
+    assert mutated != src
+    csrc = tmp_path / "mutant.c"
+    csrc.write_text(mutated)
+    so = tmp_path / "libmutant.so"
+    oracle.build(str(csrc), str(so))
+    lib = oracle.load(str(so))
+    caught = []
+    for pin in catchers:
+        try:
+            pin(lib)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"mutant {name} passed every pin it should fail"
