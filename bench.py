@@ -1,0 +1,423 @@
+"""Benchmark: single-GPU MoE plan -> dispatch -> combine.
+
+One step = moe_plan + moe_dispatch + moe_combine over one batch of the
+MoonEP-shaped workload (S=4096 tokens, H=7168, E=64 experts, K=8, bf16,
+uniform top-8, softmax weights; the expert output rows y are produced once,
+untimed, by the synthetic expert stage y = bf16(x * c_e)).  L2 is flushed
+(a 512 MiB write) before every timed step; step time is measured with CUDA
+events on the launching stream.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  `value` = algorithmic bytes of plan + dispatch +
+combine per step / mean step time, summed over ranks (replicas: every rank
+runs its own batch; no data moves between GPUs).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "dispatch & combine GB/s and % HBM roofline at S=4096 H=7168 E=64 K=8; µs/call"
+WORKLOAD = "moonep"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (what the method must move; scratch traffic not counted)
+# ---------------------------------------------------------------------------
+
+def algorithmic_bytes(S, H, E, K, V, elem=2, out_elem=2):
+    plan = S * K * 4 + E * 4 + (E + 1) * 8 + V * 4 + S * K * 8 + 4
+    dispatch = S * H * elem + S * K * 8 + V * H * elem
+    combine = V * H * elem + S * K * (8 + 4) + S * H * out_elem
+    return {"plan": plan, "dispatch": dispatch, "combine": combine}
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of that kernel; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        ent = t[kernel]
+        src = os.path.join(ROOT, "combine_moe_plan_02_gb300", "csrc", ent["source"])
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if digest != ent["sha256"]:
+            return None
+        return float(ent["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+CLOCK_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                "clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, device_index: int, interval_ms: int = 50):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(device_index), f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(interval_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# multi-rank helpers (replicas; also exercised with gloo on CPU in the tests)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(elapsed_ms: float, local_bytes: float, world: int, device=None):
+    """Max of the timed region over ranks and the sum of bytes processed."""
+    if world == 1:
+        return elapsed_ms, local_bytes
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+    b = torch.tensor([local_bytes], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(b.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+
+ORACLE_SAMPLE_TOKENS = 1024
+
+
+def oracle_sample(seed: int = 0):
+    """A bounded sample of the workload: the first 1024 tokens of the batch,
+    with the expert output rows prepared once."""
+    import oracle
+    wl = workloads.make(WORKLOAD, seed=seed)
+    n = ORACLE_SAMPLE_TOKENS
+    wl.S = n
+    wl.topk_idx = np.ascontiguousarray(wl.topk_idx[:n])
+    wl.topk_w = np.ascontiguousarray(wl.topk_w[:n])
+    wl.x = np.ascontiguousarray(wl.x[:n])
+    p = oracle.plan(wl.topk_idx, wl.E)
+    V = int(p["off"][-1])
+    packed = oracle.dispatch(wl.x, p["tok_map"], V)
+    y = oracle.expert_scale_bf16(packed, p["off"], wl.expert_scale)
+    return wl, y, V
+
+
+def oracle_step(wl, y, V):
+    import oracle
+    p = oracle.plan(wl.topk_idx, wl.E)
+    oracle.dispatch(wl.x, p["tok_map"], V)
+    oracle.combine(y, "bf16", wl.topk_w, p["tok_map"], wl.H, "bf16")
+
+
+def cpu_baseline(min_seconds: float = 10.0, max_passes: int = 200):
+    wl, y, V = oracle_sample()
+    by = sum(algorithmic_bytes(wl.S, wl.H, wl.E, wl.K, V).values())
+    oracle_step(wl, y, V)  # warm
+    t0 = time.perf_counter()
+    n = 0
+    while n < max_passes:
+        oracle_step(wl, y, V)
+        n += 1
+        if time.perf_counter() - t0 >= min_seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": by * n / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {ORACLE_SAMPLE_TOKENS} of the 4096 tokens (H=7168 E=64 K=8 bf16), "
+                      f"plan+dispatch+combine, {n} passes in {dt:.1f} s, single-threaded C oracle",
+            "seconds": round(dt, 2)}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    wl, y, V = oracle_sample()
+    by = sum(algorithmic_bytes(wl.S, wl.H, wl.E, wl.K, V).values())
+    for _ in range(args.warmup):
+        oracle_step(wl, y, V)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(wl, y, V)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = by / (ms / 1e3) / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: first {ORACLE_SAMPLE_TOKENS} tokens of S=4096 "
+                               "H=7168 E=64 K=8 bf16 per step (CPU oracle)",
+                   "S": ORACLE_SAMPLE_TOKENS, "H": wl.H, "E": wl.E, "K": wl.K},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"first {ORACLE_SAMPLE_TOKENS} tokens per step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU leg
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+
+    import combine_moe_plan_02_gb300 as moe
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    moe.lib()
+
+    wl = workloads.make(WORKLOAD, seed=rank)
+    S, H, E, K = wl.S, wl.H, wl.E, wl.K
+    stream = torch.cuda.current_stream(dev)
+
+    # device-resident inputs and preallocated outputs
+    idx = torch.from_numpy(wl.topk_idx).to(dev)
+    w = torch.from_numpy(wl.topk_w).to(dev)
+    x = torch.from_numpy(wl.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    plan = moe.Plan(torch.empty(E, dtype=torch.int32, device=dev),
+                    torch.empty(E + 1, dtype=torch.int64, device=dev),
+                    torch.empty(S * K, dtype=torch.int32, device=dev),
+                    torch.empty(S, K, dtype=torch.int64, device=dev),
+                    torch.empty(1, dtype=torch.int32, device=dev))
+    ws = torch.empty(max(moe.moe_plan_workspace_size(S, K, E), 256), dtype=torch.uint8, device=dev)
+    packed = torch.empty(S * K, H, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(S, H, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    # expert output rows, produced once (untimed): y = bf16(f32(x) * c_e)
+    moe.moe_plan(idx, E, out=plan, workspace=ws)
+    moe.moe_dispatch(x, plan.tok_map, packed_x=packed)
+    c_row = torch.repeat_interleave(torch.from_numpy(wl.expert_scale).to(dev), plan.cnt.long())
+    y = (packed.float() * c_row[:, None]).to(torch.bfloat16)
+    torch.cuda.synchronize()
+    V = int(plan.off[-1].item())
+    nby = algorithmic_bytes(S, H, E, K, V)
+    step_bytes = sum(nby.values())
+    launches_per_step = (2 if moe.moe_plan_workspace_size(S, K, E) > 0 else 1) + 1 + 1
+
+    def step():
+        moe.moe_plan(idx, E, out=plan, workspace=ws, stream=stream)
+        moe.moe_dispatch(x, plan.tok_map, packed_x=packed, stream=stream)
+        moe.moe_combine(y, w, plan.tok_map, out=out, stream=stream)
+
+    sampler = ClockSampler(dev.index)
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+
+    n = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        e = ev[i]
+        e[0].record(stream)
+        moe.moe_plan(idx, E, out=plan, workspace=ws, stream=stream)
+        e[1].record(stream)
+        moe.moe_dispatch(x, plan.tok_map, packed_x=packed, stream=stream)
+        e[2].record(stream)
+        moe.moe_combine(y, w, plan.tok_map, out=out, stream=stream)
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    barrier(world, dev)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+
+    t_plan = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)]
+    t_disp = [ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]
+    t_comb = [ev[i][2].elapsed_time(ev[i][3]) for i in range(n)]
+    t_step = [ev[i][0].elapsed_time(ev[i][3]) for i in range(n)]
+    local_ms = sum(t_step)
+    max_ms, tot_bytes = aggregate(local_ms, step_bytes * n, world, dev)
+    ms_per_step = max_ms / n
+    value = tot_bytes / (max_ms / 1e3) / 1e9
+
+    # e2e: host (pinned) inputs -> GPU path -> host output, copies timed
+    h_idx = torch.from_numpy(wl.topk_idx).pin_memory()
+    h_w = torch.from_numpy(wl.topk_w).pin_memory()
+    h_x = torch.from_numpy(wl.x.view(np.int16)).pin_memory()
+    h_out = torch.empty(S, H, dtype=torch.int16).pin_memory()
+    d_x16 = x.view(torch.int16)
+
+    def e2e_step():
+        idx.copy_(h_idx, non_blocking=True)
+        w.copy_(h_w, non_blocking=True)
+        d_x16.copy_(h_x, non_blocking=True)
+        step()
+        h_out.copy_(out.view(torch.int16), non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+    barrier(world, dev)
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        e2e_ev[i][0].record(stream)
+        e2e_step()
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world, dev)
+    e2e_local = sum(a.elapsed_time(b) for a, b in e2e_ev)
+    e2e_max, e2e_bytes = aggregate(e2e_local, step_bytes * n, world, dev)
+    assert np.array_equal(h_out.numpy(), out.view(torch.int16).cpu().numpy())
+
+    peak, peak_kind = read_peaks()
+    disp_ms = statistics.mean(t_disp)
+    comb_ms = statistics.mean(t_comb)
+    dom = "dispatch" if disp_ms >= comb_ms else "combine"
+    dom_ms = disp_ms if dom == "dispatch" else comb_ms
+    achieved = nby[dom] / (dom_ms / 1e3) / 1e9
+
+    def percall(name, ts):
+        m = statistics.mean(ts)
+        gbs = nby[name] / (m / 1e3) / 1e9
+        return {"us": round(1e3 * m, 2), "us_median": round(1e3 * statistics.median(ts), 2),
+                "us_min": round(1e3 * min(ts), 2), "GB_per_s": round(gbs, 1),
+                "frac_of_peak": round(gbs / peak, 4), "algorithmic_bytes": nby[name]}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": n,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "moonep: S=4096 H=7168 E=64 K=8 bf16, uniform distinct top-8, "
+                               "softmax(N(0,1)) weights, per-expert scale c_e~U(0.5,1.5)",
+                   "S": S, "H": H, "E": E, "K": K, "valid_rows": V,
+                   "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "per_call": {"plan": percall("plan", t_plan), "dispatch": percall("dispatch", t_disp),
+                     "combine": percall("combine", t_comb)},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": f"{peak_kind} copy bandwidth (burst)",
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": kernel_traffic(dom)},
+        "e2e": {"value": e2e_bytes / (e2e_max / 1e3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_max / n,
+                "h2d_bytes_per_step": int(h_idx.numel() * 4 + h_w.numel() * 4 + h_x.numel() * 2),
+                "d2h_bytes_per_step": int(h_out.numel() * 2)},
+        "gpu_launches": launches_per_step * n,
+        "wall_s_timed": round(wall, 4),
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+        line["cpu_baseline"]["host_cpus"] = os.cpu_count()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the timed CPU oracle leg (profiling runs)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,309 @@
+// Combine: gather each token's K expert-output rows, weighted f32 sum.
+//
+// Sources: ROCm/mori "Draft: cco + flydsl dispatch/combine #448": PR
+// description (gather each token's k expert outputs and reduce in f32),
+// StdMoE note (convert_combine_input = sum_k wts[k]*packed_x[slot_k]; the
+// gather combine then sums over destinations), accumulator note (bf16 and
+// f32 inputs widened to f32).  ROCm/mori "EPv2 internode dispatch/combine
+// over CCO/GDA", combine note: 16-byte load-first gathers, and warp slices
+// sized to whole vector steps so that no warp runs a scalar tail.
+//
+// GB300 design: the work unit is (output row, slice); a slice is 32 lanes x
+// R steps of 8 elements (16 bytes of bf16 or 32 bytes of f32 per k).  A warp
+// reads the row's K map entries and weights once (lane k holds entry k,
+// shuffled to all lanes), then per step issues all K 16-byte gathers before
+// the first add (load first), accumulates in f32 in increasing k with a
+// separately rounded multiply and add, and stores the rounded result with
+// one 16-byte store.  A persistent grid sized to the SM count strides over
+// units.  There is no shared memory, no atomics and no inter-CTA wait.
+
+#include "common.cuh"
+
+#include <cuda_bf16.h>
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kKChunk = 8;   // map entries held in registers at a time
+
+enum WMode { kWeightDirect = 0, kWeightViaSrc = 1, kUnweighted = 2 };
+
+__device__ uint32_t g_combine_error;  // kErrCombineIndex
+
+struct CombineArgs {
+    const uint8_t *y;          // input rows
+    const float *w;            // [*, K] weights (unless unweighted)
+    const int32_t *wsrc;       // kWeightViaSrc: weight row = wsrc[i] / K
+    const int64_t *map;        // [rows, K] input row or -1
+    int64_t rows;              // output rows (host bound)
+    const int64_t *rows_dev;   // if set: rows = min(*rows_dev, rows)
+    int64_t y_rows;            // rows of y (bounds check)
+    int64_t w_rows;            // rows of w (bounds check, kWeightViaSrc)
+    int K;
+    int64_t H;                 // elements per row (multiple of 8)
+    int64_t steps;             // H / 8
+    int R;                     // steps per lane per unit
+    int slices;                // units per row
+    uint8_t *out;
+};
+
+template <typename T> struct Io;
+
+template <> struct Io<__nv_bfloat16> {
+    static constexpr int kVec = 1;  // 16-byte vectors per 8 elements
+    __device__ __forceinline__ static void load(uint4 (&v)[1], const uint8_t *row, int64_t p)
+    {
+        v[0] = ld_stream16(row + p * 16);
+    }
+    __device__ __forceinline__ static void widen(const uint4 (&v)[1], float (&f)[8])
+    {
+        const uint32_t u[4] = {v[0].x, v[0].y, v[0].z, v[0].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            f[2 * q] = __uint_as_float(u[q] << 16);
+            f[2 * q + 1] = __uint_as_float(u[q] & 0xffff0000u);
+        }
+    }
+    __device__ __forceinline__ static void store(uint8_t *out_row, int64_t p, const float (&f)[8])
+    {
+        uint32_t u[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * q], f[2 * q + 1]);  // RNE
+            u[q] = *reinterpret_cast<uint32_t *>(&b);
+        }
+        st16(out_row + p * 16, make_uint4(u[0], u[1], u[2], u[3]));
+    }
+};
+
+template <> struct Io<float> {
+    static constexpr int kVec = 2;
+    __device__ __forceinline__ static void load(uint4 (&v)[2], const uint8_t *row, int64_t p)
+    {
+        v[0] = ld_stream16(row + p * 32);
+        v[1] = ld_stream16(row + p * 32 + 16);
+    }
+    __device__ __forceinline__ static void widen(const uint4 (&v)[2], float (&f)[8])
+    {
+        f[0] = __uint_as_float(v[0].x); f[1] = __uint_as_float(v[0].y);
+        f[2] = __uint_as_float(v[0].z); f[3] = __uint_as_float(v[0].w);
+        f[4] = __uint_as_float(v[1].x); f[5] = __uint_as_float(v[1].y);
+        f[6] = __uint_as_float(v[1].z); f[7] = __uint_as_float(v[1].w);
+    }
+    __device__ __forceinline__ static void store(uint8_t *out_row, int64_t p, const float (&f)[8])
+    {
+        st16(out_row + p * 32, make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                                          __float_as_uint(f[2]), __float_as_uint(f[3])));
+        st16(out_row + p * 32 + 16, make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]),
+                                               __float_as_uint(f[6]), __float_as_uint(f[7])));
+    }
+};
+
+template <typename Tin, typename Tout, int WM>
+__global__ void __launch_bounds__(kThreads, 2) combine_kernel(CombineArgs a)
+{
+    griddep_wait();  // y, map, weights come from earlier stream work
+    griddep_launch_dependents();
+
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+    const int64_t W = ((int64_t)gridDim.x * kThreads) >> 5;
+    const int64_t rows = a.rows_dev ? min(*a.rows_dev, a.rows) : a.rows;
+    const int64_t units = rows * a.slices;
+    const int K = a.K;
+    constexpr int kInBytes = (int)sizeof(Tin) * 8;    // bytes of 8 input elements
+    constexpr int kOutBytes = (int)sizeof(Tout) * 8;
+    const int64_t in_row_bytes = a.steps * kInBytes;
+    const int64_t out_row_bytes = a.steps * kOutBytes;
+
+    for (int64_t u = gw; u < units; u += W) {
+        const int64_t i = u / a.slices;
+        const int sl = (int)(u - i * a.slices);
+        // this lane's map entry and weight (lane k <-> entry k)
+        int64_t my_row = -1;
+        float my_w = 1.0f;
+        if (lane < K) {
+            my_row = __ldg(a.map + i * K + lane);
+            int64_t wr = i;
+            if (WM == kWeightViaSrc) wr = (int64_t)(__ldg(a.wsrc + i) / K);
+            const bool ok = my_row >= -1 && my_row < a.y_rows && (WM != kWeightViaSrc ||
+                                                                 (wr >= 0 && wr < a.w_rows));
+            if (!ok) {
+                // never gather outside the buffers: drop the term and report
+                atomicOr(&g_combine_error, kErrCombineIndex);
+                my_row = -1;
+            } else if (WM != kUnweighted && my_row >= 0) {
+                my_w = __ldg(a.w + wr * K + lane);
+            }
+        }
+        const int64_t pbase = (int64_t)sl * 32 * a.R;
+        uint8_t *out_row = a.out + i * out_row_bytes;
+
+        // the trip count is the same for every lane (shuffles below need the
+        // whole warp); lanes past the end of the row are predicated off
+        for (int r = 0; r < a.R; ++r) {
+            const int64_t p = pbase + (int64_t)r * 32 + lane;
+            const bool active = p < a.steps;
+            float acc[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+            for (int k0 = 0; k0 < K; k0 += kKChunk) {
+                // load first: every gather of this chunk of k is in flight
+                // before the first add
+                uint4 v[kKChunk][Io<Tin>::kVec];
+                int64_t rk[kKChunk];
+#pragma unroll
+                for (int kk = 0; kk < kKChunk; ++kk) {
+                    rk[kk] = __shfl_sync(0xffffffffu, my_row, (k0 + kk) & 31);
+                    if (active && k0 + kk < K && rk[kk] >= 0)
+                        Io<Tin>::load(v[kk], a.y + rk[kk] * in_row_bytes, p);
+                }
+#pragma unroll
+                for (int kk = 0; kk < kKChunk; ++kk) {
+                    const float wk = __shfl_sync(0xffffffffu, my_w, (k0 + kk) & 31);
+                    if (active && k0 + kk < K && rk[kk] >= 0) {
+                        float f[8];
+                        Io<Tin>::widen(v[kk], f);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            if (WM == kUnweighted)
+                                acc[q] = __fadd_rn(acc[q], f[q]);
+                            else
+                                acc[q] = __fadd_rn(acc[q], __fmul_rn(wk, f[q]));
+                        }
+                    }
+                }
+            }
+            if (active) Io<Tout>::store(out_row, p, acc);
+        }
+    }
+}
+
+template <typename Tin, typename Tout>
+void (*pick_kernel(int wm))(CombineArgs)
+{
+    switch (wm) {
+    case kWeightDirect: return combine_kernel<Tin, Tout, kWeightDirect>;
+    case kWeightViaSrc: return combine_kernel<Tin, Tout, kWeightViaSrc>;
+    default: return combine_kernel<Tin, Tout, kUnweighted>;
+    }
+}
+
+void (*select_kernel(int in_dt, int out_dt, int wm))(CombineArgs)
+{
+    if (in_dt == MOE_BF16 && out_dt == MOE_BF16) return pick_kernel<__nv_bfloat16, __nv_bfloat16>(wm);
+    if (in_dt == MOE_BF16 && out_dt == MOE_F32) return pick_kernel<__nv_bfloat16, float>(wm);
+    if (in_dt == MOE_F32 && out_dt == MOE_BF16) return pick_kernel<float, __nv_bfloat16>(wm);
+    if (in_dt == MOE_F32 && out_dt == MOE_F32) return pick_kernel<float, float>(wm);
+    return nullptr;
+}
+
+int launch_combine(CombineArgs &a, int in_dt, int out_dt, int wm, cudaStream_t stream)
+{
+    void (*fn)(CombineArgs) = select_kernel(in_dt, out_dt, wm);
+    if (!fn) return MOE_EINVAL;
+    // slices: at most 8 steps per lane per unit, slices of equal size
+    const int64_t lane_steps = (a.steps + 31) / 32;
+    a.slices = (int)((lane_steps + 7) / 8);
+    a.R = (int)((lane_steps + a.slices - 1) / a.slices);
+    int per_sm = 0;
+    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, 0);
+    if (err != cudaSuccess || per_sm < 1) {
+        set_cuda_error(err != cudaSuccess ? err : cudaErrorInvalidConfiguration);
+        return MOE_ECUDA;
+    }
+    const int64_t units = a.rows * a.slices;
+    int64_t blocks = (units + kThreads / 32 - 1) / (kThreads / 32);
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    err = launch_pdl(fn, dim3((unsigned)blocks), dim3(kThreads), 0, stream, a);
+    if (err != cudaSuccess) {
+        set_cuda_error(err);
+        return MOE_ECUDA;
+    }
+    return check_launch();
+}
+
+bool combine_dtype_ok(int dt) { return dt == MOE_BF16 || dt == MOE_F32; }
+
+} // namespace
+} // namespace moe
+
+using namespace moe;
+
+MOE_EXPORT int moe_combine(const void *y, int in_dtype, const float *topk_w,
+                           const int64_t *tok_map, int64_t S, int64_t H, int K, void *out,
+                           int out_dtype, moe_stream_t stream)
+{
+    if (!combine_dtype_ok(in_dtype) || !combine_dtype_ok(out_dtype)) return MOE_EINVAL;
+    if (S < 0 || H < 1 || K < 1 || K > 32) return MOE_EINVAL;
+    if (S == 0) return MOE_OK;
+    if (!y || !topk_w || !tok_map || !out) return MOE_EINVAL;
+    if (H % 8 || !aligned16(y) || !aligned16(out)) return MOE_EALIGN;
+    CombineArgs a = {};
+    a.y = static_cast<const uint8_t *>(y);
+    a.w = topk_w;
+    a.map = tok_map;
+    a.rows = S;
+    a.y_rows = S * (int64_t)K;
+    a.K = K;
+    a.H = H;
+    a.steps = H / 8;
+    a.out = static_cast<uint8_t *>(out);
+    return launch_combine(a, in_dtype, out_dtype, kWeightDirect, (cudaStream_t)stream);
+}
+
+MOE_EXPORT int moe_combine_dedup(const void *y, int in_dtype, const float *topk_w,
+                                 const int64_t *goff, int G, const int32_t *grp_src,
+                                 const int64_t *grp_tok_map, const int64_t *gtok_map, int64_t S,
+                                 int64_t H, int K, int64_t max_rows, float *gtok, void *out,
+                                 int out_dtype, moe_stream_t stream)
+{
+    if (!combine_dtype_ok(in_dtype) || !combine_dtype_ok(out_dtype)) return MOE_EINVAL;
+    if (S < 0 || H < 1 || K < 1 || K > 32 || G < 1 || G > 1024) return MOE_EINVAL;
+    if (S == 0) return MOE_OK;
+    if (!y || !topk_w || !goff || !grp_src || !grp_tok_map || !gtok_map || !gtok || !out)
+        return MOE_EINVAL;
+    if (max_rows < S * (int64_t)(K < G ? K : G)) return MOE_EINVAL;
+    if (H % 8 || !aligned16(y) || !aligned16(out) || !aligned16(gtok)) return MOE_EALIGN;
+    // stage 1: per group row, weighted sum of its experts' outputs (f32)
+    CombineArgs a = {};
+    a.y = static_cast<const uint8_t *>(y);
+    a.w = topk_w;
+    a.wsrc = grp_src;
+    a.map = grp_tok_map;
+    a.rows = max_rows;
+    a.rows_dev = goff + G;
+    a.y_rows = S * (int64_t)K;
+    a.w_rows = S;
+    a.K = K;
+    a.H = H;
+    a.steps = H / 8;
+    a.out = reinterpret_cast<uint8_t *>(gtok);
+    if (int rc = launch_combine(a, in_dtype, MOE_F32, kWeightViaSrc, (cudaStream_t)stream))
+        return rc;
+    // stage 2: per token, unweighted sum of its group rows
+    CombineArgs b = {};
+    b.y = reinterpret_cast<const uint8_t *>(gtok);
+    b.map = gtok_map;
+    b.rows = S;
+    b.y_rows = max_rows;
+    b.K = K;
+    b.H = H;
+    b.steps = H / 8;
+    b.out = static_cast<uint8_t *>(out);
+    return launch_combine(b, MOE_F32, out_dtype, kUnweighted, (cudaStream_t)stream);
+}
+
+namespace moe {
+// Reads and clears this file's device error bits.
+cudaError_t read_combine_errors(uint32_t *flags)
+{
+    uint32_t zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(flags, g_combine_error, sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_combine_error, &zero, sizeof(uint32_t));
+    return e;
+}
+} // namespace moe

@@ -1,0 +1,397 @@
+// Plan: per-expert histogram, exclusive scan and stable slot assignment.
+//
+// Sources: ROCm/mori "Draft: cco + flydsl dispatch/combine #448", StdMoE note
+// (packed_cnt / packed_src / i64 slot map with -1) and routing-handle note
+// (local_expert_count); the same page's PR description (ballot dedup per
+// destination) for the group plan.  The pages hand out slots with atomics;
+// here the slot of entry (s,k) is its rank among earlier entries of the same
+// expert in (token, k) order, so the map is a pure function of topk_idx.
+//
+// Design (no inter-CTA spin waits and no cooperative launch: every CTA is
+// independent, as MoonEP "Drop cooperative launch from the CTA-independent
+// local kernels" argues for local kernels):
+//   the flat entry list i = s*K + k is cut into T tiles of `tile` entries;
+//   a tile is cut into 32 warp sub-tiles of `sub` entries, walked in chunks
+//   of 32 consecutive entries (one per lane).
+//   kernel 1 (only when T > 1): per-tile key histograms -> workspace
+//     [T][nkeys + 1] (last column: invalid entries).
+//   kernel 2, one CTA per tile:
+//     (a) per-warp key counts: lanes holding the same key find each other
+//         with __match_any_sync and the lowest lane adds the group size;
+//     (b) programmatic-dependent-launch wait, then the tile histograms give
+//         the global counts and the counts of earlier tiles;
+//     (c) a block scan over keys gives off[];
+//     (d) a scan over the 32 warps per key gives each warp's base;
+//     (e) the warps walk their chunks again: rank = warp base + running
+//         count + popc(match mask & lanemask_lt).
+//   With T == 1 kernel 2 runs alone and takes the counts from (a).
+// The group plan (dedup) runs the same two kernels on the key "group of
+// the entry, if it is its token's first entry in that group".
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+constexpr int64_t kSingleTileMax = 8192;   // entries handled by one CTA alone
+constexpr int64_t kMaxTiles = 128;
+
+struct PlanGeom {
+    int64_t n;      // entries S*K
+    int64_t tile;   // entries per tile (multiple of kThreads)
+    int64_t sub;    // entries per warp sub-tile (multiple of 32)
+    int T;          // tiles
+};
+
+PlanGeom plan_geom(int64_t S, int K)
+{
+    PlanGeom g;
+    g.n = S * (int64_t)K;
+    int64_t tile;
+    if (g.n <= kSingleTileMax) {
+        tile = (g.n + kThreads - 1) / kThreads * kThreads;
+        if (tile == 0) tile = kThreads;
+    } else {
+        int64_t want = (g.n + kMaxTiles - 1) / kMaxTiles;
+        tile = (want + kThreads - 1) / kThreads * kThreads;
+        if (tile < 2 * kThreads) tile = 2 * kThreads;
+    }
+    g.tile = tile;
+    g.sub = tile / kWarps;
+    g.T = (int)((g.n + tile - 1) / tile);
+    if (g.T == 0) g.T = 1;
+    return g;
+}
+
+size_t hist_ws_bytes(const PlanGeom &g, int nkeys)
+{
+    if (g.T <= 1) return 0;
+    size_t b = (size_t)g.T * (size_t)(nkeys + 1) * sizeof(int32_t);
+    return (b + 255) / 256 * 256;
+}
+
+struct RankOut {
+    int32_t *cnt;          // [nkeys]
+    int64_t *off;          // [nkeys + 1]
+    int64_t *map;          // [n]
+    int32_t *src;          // [n]
+    int32_t *n_invalid;    // [1] (direct plan) or null
+    const int64_t *tok_map;  // group plan: tok_map of the direct plan
+    int64_t *grp_tok_map;    // group plan: [rows, K]
+};
+
+// Key of the 32 entries [c, c+32) of a chunk, one per lane: the slot key, -1
+// for an entry that takes no slot, -2 for a lane past the end.  All lanes of
+// the warp call it together.
+struct DirectKey {
+    const int32_t *idx;
+    int E;
+    static constexpr bool kCountsInvalid = true;
+    __device__ __forceinline__ int chunk_key(int64_t i, bool in_range) const
+    {
+        if (!in_range) return -2;
+        int e = __ldg(idx + i);
+        return (e >= 0 && e < E) ? e : -1;
+    }
+    __device__ __forceinline__ void emit(int64_t, int64_t, int, const RankOut &) const {}
+};
+
+struct GroupKey {
+    const int32_t *idx;
+    int E, K, gs;
+    static constexpr bool kCountsInvalid = false;
+    __device__ __forceinline__ int group(int64_t i) const
+    {
+        int e = __ldg(idx + i);
+        return (e >= 0 && e < E) ? e / gs : -1;
+    }
+    __device__ __forceinline__ int chunk_key(int64_t i, bool in_range) const
+    {
+        int g = in_range ? group(i) : -1;
+        const int lane = threadIdx.x & 31;
+        if ((32 % K) == 0) {
+            // Chunks start at multiples of 32, so a token's K entries sit in
+            // one chunk: ballot dedup over (token, group) inside the warp.
+            const int tok = lane / K;
+            unsigned peers = __match_any_sync(0xffffffffu, g < 0 ? -1 - lane : tok * 4096 + g);
+            if (!in_range) return -2;
+            return (g >= 0 && lane == __ffs(peers) - 1) ? g : -1;
+        }
+        if (!in_range) return -2;
+        if (g < 0) return -1;
+        const int64_t s0 = i - i % K;
+        for (int64_t j = s0; j < i; ++j)
+            if (group(j) == g) return -1;
+        return g;
+    }
+    // A representative lists its token's experts that fall in its group.
+    __device__ __forceinline__ void emit(int64_t i, int64_t row, int g, const RankOut &o) const
+    {
+        const int64_t s0 = i - i % K;
+        for (int kk = 0; kk < K; ++kk)
+            o.grp_tok_map[row * K + kk] = (group(s0 + kk) == g) ? o.tok_map[s0 + kk] : -1;
+    }
+};
+
+// Kernel 1: histogram of tile t into ws[t * (nkeys + 1) + key]; invalid
+// entries into ws[t * (nkeys + 1) + nkeys].
+template <typename Key>
+__global__ void __launch_bounds__(kThreads, 1) plan_hist_kernel(Key key, int nkeys, PlanGeom g,
+                                                             int32_t *__restrict__ ws)
+{
+    extern __shared__ int32_t s_hist[];  // [nkeys + 1]
+    griddep_launch_dependents();
+    for (int e = threadIdx.x; e <= nkeys; e += kThreads) s_hist[e] = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t = blockIdx.x;
+    const int64_t wbegin = (int64_t)t * g.tile + (int64_t)warp * g.sub;
+    const int64_t wend = min(wbegin + g.sub, g.n);
+    int invalid = 0;
+    for (int64_t c = wbegin; c < wend; c += 32) {
+        const int64_t i = c + lane;
+        int k = key.chunk_key(i, i < wend);
+        if (k == -1) ++invalid;
+        unsigned peers = __match_any_sync(0xffffffffu, k);
+        if (k >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_hist[k], __popc(peers));
+    }
+    if (Key::kCountsInvalid) {
+        for (int o = 16; o; o >>= 1) invalid += __shfl_xor_sync(0xffffffffu, invalid, o);
+        if (lane == 0 && invalid) atomicAdd(&s_hist[nkeys], invalid);
+    }
+    __syncthreads();
+    int32_t *row = ws + (int64_t)t * (nkeys + 1);
+    for (int e = threadIdx.x; e <= nkeys; e += kThreads) row[e] = s_hist[e];
+}
+
+// Exclusive scan of v over the block; returns this thread's exclusive
+// prefix and sets `total`.
+__device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t *s_warp, int64_t &total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int64_t x = v;
+    for (int o = 1; o < 32; o <<= 1) {
+        int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int64_t w = s_warp[lane];
+        for (int o = 1; o < 32; o <<= 1) {
+            int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        s_warp[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    total = s_warp[kWarps - 1];
+    const int64_t before = warp ? s_warp[warp - 1] : 0;
+    return before + x - v;
+}
+
+// Kernel 2: stable ranks of one tile (steps (a)-(e) of the file comment).
+template <typename Key>
+__global__ void __launch_bounds__(kThreads, 1) plan_rank_kernel(Key key, int nkeys, PlanGeom g,
+                                                             const int32_t *__restrict__ ws,
+                                                             RankOut o)
+{
+    extern __shared__ int32_t smem[];
+    int32_t *s_wc = smem;                               // [kWarps][nkeys]
+    int64_t *s_base = reinterpret_cast<int64_t *>(s_wc + ((kWarps * nkeys + 1) & ~1));  // [nkeys]
+    int32_t *s_tot = reinterpret_cast<int32_t *>(s_base + nkeys);                     // [nkeys]
+    int32_t *s_bef = s_tot + nkeys;                                                   // [nkeys]
+    __shared__ int64_t s_scan[kWarps];
+    __shared__ int32_t s_inval;
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t = blockIdx.x;
+    const bool single = (g.T == 1);
+
+    griddep_launch_dependents();
+    // With one tile nothing of this plan ran before: wait for whatever wrote
+    // topk_idx.  With several, kernel 1 was launched without the attribute,
+    // so it (and this kernel) began only after earlier stream work finished.
+    if (single) griddep_wait();
+
+    for (int i = threadIdx.x; i < kWarps * nkeys; i += kThreads) s_wc[i] = 0;
+    for (int i = threadIdx.x; i < nkeys; i += kThreads) s_tot[i] = s_bef[i] = 0;
+    if (threadIdx.x == 0) s_inval = 0;
+    __syncthreads();
+
+    const int64_t wbegin = (int64_t)t * g.tile + (int64_t)warp * g.sub;
+    const int64_t wend = min(wbegin + g.sub, g.n);
+    int32_t *my_wc = s_wc + warp * nkeys;
+
+    // (a) per-warp counts
+    int invalid = 0;
+    for (int64_t c = wbegin; c < wend; c += 32) {
+        const int64_t i = c + lane;
+        const int k = key.chunk_key(i, i < wend);
+        if (k == -1) ++invalid;
+        const unsigned peers = __match_any_sync(0xffffffffu, k);
+        if (k >= 0 && lane == __ffs(peers) - 1) my_wc[k] += __popc(peers);
+        __syncwarp();
+    }
+    if (Key::kCountsInvalid && single) {
+        for (int sh = 16; sh; sh >>= 1) invalid += __shfl_xor_sync(0xffffffffu, invalid, sh);
+        if (lane == 0 && invalid) atomicAdd(&s_inval, invalid);
+    }
+
+    // (b) global counts and counts of earlier tiles
+    if (single) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < nkeys; e += kThreads) {
+            int32_t tot = 0;
+            for (int w = 0; w < kWarps; ++w) tot += s_wc[w * nkeys + e];
+            s_tot[e] = tot;
+        }
+    } else {
+        griddep_wait();  // tile histograms of kernel 1 are complete and visible
+        const int stride = nkeys + 1;
+        const int64_t nws = (int64_t)g.T * stride;
+#pragma unroll 4
+        for (int64_t j = threadIdx.x; j < nws; j += kThreads) {
+            const int tt = (int)(j / stride);
+            const int e = (int)(j - (int64_t)tt * stride);
+            const int32_t h = ws[j];
+            if (e < nkeys) {
+                atomicAdd(&s_tot[e], h);
+                if (tt < t) atomicAdd(&s_bef[e], h);
+            } else if (Key::kCountsInvalid && t == 0) {
+                atomicAdd(&s_inval, h);
+            }
+        }
+    }
+    __syncthreads();
+
+    // (c) exclusive scan over keys (nkeys <= kThreads: one key per thread)
+    const int e = threadIdx.x;
+    const int64_t tot = (e < nkeys) ? s_tot[e] : 0;
+    int64_t total;
+    const int64_t offe = block_exclusive_scan(tot, s_scan, total);
+    if (e < nkeys) {
+        s_base[e] = offe + s_bef[e];
+        if (t == 0) {
+            o.cnt[e] = (int32_t)tot;
+            o.off[e] = offe;
+        }
+    }
+    if (t == 0 && threadIdx.x == 0) {
+        o.off[nkeys] = total;
+        if (o.n_invalid) *o.n_invalid = s_inval;
+    }
+
+    // (d) exclusive scan over warps, per key, relative to the tile base
+    if (e < nkeys) {
+        int32_t run = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            const int32_t c = s_wc[w * nkeys + e];
+            s_wc[w * nkeys + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+
+    // (e) assign ranks
+    for (int64_t c = wbegin; c < wend; c += 32) {
+        const int64_t i = c + lane;
+        const int k = key.chunk_key(i, i < wend);
+        const unsigned peers = __match_any_sync(0xffffffffu, k);
+        int64_t row = -1;
+        if (k >= 0) row = s_base[k] + my_wc[k] + __popc(peers & lanemask_lt());
+        __syncwarp();
+        if (k >= 0 && lane == __ffs(peers) - 1) my_wc[k] += __popc(peers);
+        __syncwarp();
+        if (i < wend) {
+            o.map[i] = row;
+            if (row >= 0) {
+                o.src[row] = (int32_t)i;
+                key.emit(i, row, k, o);
+            }
+        }
+    }
+}
+
+template <typename Key>
+int run_plan(Key key, int nkeys, const PlanGeom &g, const RankOut &o, void *ws,
+             size_t ws_bytes, cudaStream_t stream)
+{
+    const size_t need = hist_ws_bytes(g, nkeys);
+    if (need > 0 && (ws == nullptr || ws_bytes < need)) return MOE_EINVAL;
+    if (need > 0 && (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOE_EALIGN;
+    if (g.T > 1) {
+        const size_t smem1 = (size_t)(nkeys + 1) * sizeof(int32_t);
+        plan_hist_kernel<Key><<<g.T, kThreads, smem1, stream>>>(key, nkeys, g,
+                                                                 static_cast<int32_t *>(ws));
+        if (int rc = check_launch()) return rc;
+    }
+    const size_t smem2 = (size_t)((kWarps * nkeys + 1) & ~1) * sizeof(int32_t) +
+                         (size_t)nkeys * (sizeof(int64_t) + 2 * sizeof(int32_t));
+    cudaError_t err = cudaFuncSetAttribute(plan_rank_kernel<Key>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
+    if (err == cudaSuccess)
+        err = launch_pdl(plan_rank_kernel<Key>, dim3(g.T), dim3(kThreads), smem2, stream, key,
+                         nkeys, g, static_cast<const int32_t *>(ws), o);
+    if (err != cudaSuccess) {
+        set_cuda_error(err);
+        return MOE_ECUDA;
+    }
+    return check_launch();
+}
+
+int check_plan_args(int64_t S, int K, int E)
+{
+    if (S < 0 || K < 1 || K > 32 || E < 1 || E > 1024) return MOE_EINVAL;
+    if (S * (int64_t)K >= ((int64_t)1 << 31)) return MOE_EINVAL;
+    return MOE_OK;
+}
+
+} // namespace
+} // namespace moe
+
+using namespace moe;
+
+MOE_EXPORT size_t moe_plan_workspace_size(int64_t S, int K, int E)
+{
+    if (check_plan_args(S, K, E)) return 0;
+    return hist_ws_bytes(plan_geom(S, K), E);
+}
+
+MOE_EXPORT int moe_plan(const int32_t *topk_idx, int64_t S, int K, int E, int32_t *cnt,
+                        int64_t *off, int32_t *packed_src, int64_t *tok_map,
+                        int32_t *n_invalid, void *workspace, size_t workspace_bytes,
+                        moe_stream_t stream)
+{
+    if (int rc = check_plan_args(S, K, E)) return rc;
+    if (!cnt || !off || !n_invalid) return MOE_EINVAL;
+    if (S > 0 && (!topk_idx || !packed_src || !tok_map)) return MOE_EINVAL;
+    const PlanGeom g = plan_geom(S, K);
+    const DirectKey key{topk_idx, E};
+    const RankOut o{cnt, off, tok_map, packed_src, n_invalid, nullptr, nullptr};
+    return run_plan(key, E, g, o, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+MOE_EXPORT size_t moe_group_plan_workspace_size(int64_t S, int K, int E, int group_size)
+{
+    if (check_plan_args(S, K, E) || group_size < 1 || E % group_size) return 0;
+    return hist_ws_bytes(plan_geom(S, K), E / group_size);
+}
+
+MOE_EXPORT int moe_group_plan(const int32_t *topk_idx, const int64_t *tok_map, int64_t S, int K,
+                              int E, int group_size, int32_t *gcnt, int64_t *goff,
+                              int64_t *gtok_map, int32_t *grp_src, int64_t *grp_tok_map,
+                              void *workspace, size_t workspace_bytes, moe_stream_t stream)
+{
+    if (int rc = check_plan_args(S, K, E)) return rc;
+    if (group_size < 1 || E % group_size) return MOE_EINVAL;
+    if (!gcnt || !goff) return MOE_EINVAL;
+    if (S > 0 && (!topk_idx || !tok_map || !gtok_map || !grp_src || !grp_tok_map))
+        return MOE_EINVAL;
+    const PlanGeom g = plan_geom(S, K);
+    const GroupKey key{topk_idx, E, K, group_size};
+    const RankOut o{gcnt, goff, gtok_map, grp_src, nullptr, tok_map, grp_tok_map};
+    return run_plan(key, E / group_size, g, o, workspace, workspace_bytes, (cudaStream_t)stream);
+}

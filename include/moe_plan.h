@@ -1,0 +1,227 @@
+/*
+ * moe_plan.h: C ABI of the GB300 (sm_103a) MoE token dispatch / combine
+ * library (libmoe_gb300.so).
+ *
+ * One GPU holds every expert.  A step is
+ *   moe_plan      per-expert histogram, exclusive scan, stable slot map
+ *   moe_dispatch  scatter each token row into its K per-expert buckets
+ *   (expert computation by the caller: packed rows -> expert output rows y)
+ *   moe_combine   gather each token's K output rows, weighted f32 sum
+ * with a dedup variant (moe_group_plan, moe_dispatch_dedup,
+ * moe_combine_dedup) that sends each token once per virtual expert group and
+ * expands per expert from there.
+ *
+ * Sources (page title and the note on it):
+ *   ROCm/mori "Draft: cco + flydsl dispatch/combine #448": PR description
+ *     (ballot dedup, 16-byte scatter, gather combine reducing in f32), the
+ *     StdMoE note (convert_dispatch_output repacks into packed_x[expert,slot]
+ *     with packed_cnt, packed_src and an i64 slot map holding -1 for unused
+ *     entries; convert_combine_input takes sum_k wts[k]*packed_x[slot_k]),
+ *     the scale_dim note (scale rows forwarded verbatim with the token), the
+ *     routing-handle note (per-expert token count; replay with a cached map).
+ *   ROCm/mori "EPv2 internode dispatch/combine over CCO/GDA": the combine
+ *     note on 16-byte load-first gathers and warp slices of whole vector
+ *     steps; the config note requiring 16-byte token alignment.
+ *   MoonshotAI/MoonEP "Drop cooperative launch from the CTA-independent
+ *     local kernels": local kernels need no grid-wide synchronisation.
+ *
+ * Conventions for every call:
+ *   - All buffer arguments are DEVICE pointers owned by the caller; the
+ *     library allocates, frees and synchronises nothing and keeps no pointer
+ *     after a call returns.  Work is enqueued on `stream` (NULL = legacy
+ *     default stream) and runs asynchronously.
+ *   - Arrays are dense and row-major.  S = tokens, K = experts per token
+ *     (1..32), E = experts (1..1024), H = elements per row.
+ *   - Return value: MOE_OK, or an error code.  MOE_EINVAL / MOE_EALIGN are
+ *     detected on the host before anything is enqueued.  MOE_ECUDA means a
+ *     CUDA call failed; moe_last_cuda_error() returns its error code.  Data-dependent problems are never
+ *     clamped: an expert id outside [0, E) is counted in *n_invalid and its
+ *     entries are marked -1.
+ *   - S = 0 is valid: moe_plan still writes zero counts/offsets; the other
+ *     calls enqueue nothing.
+ */
+#ifndef MOE_PLAN_H
+#define MOE_PLAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moe_stream_t; /* a cudaStream_t */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_EINVAL = 1, /* null pointer, size out of range, bad dtype/group size   */
+    MOE_EALIGN = 2, /* a row pointer or row size is not a multiple of 16 bytes */
+    MOE_ECUDA = 3   /* a CUDA launch or attribute call failed                  */
+} moe_status;
+
+typedef enum {
+    MOE_BF16 = 0,    /* bfloat16, 2 bytes                                 */
+    MOE_F32 = 1,     /* IEEE binary32, 4 bytes                            */
+    MOE_FP8_E4M3 = 2 /* OCP E4M3, 1 byte (dispatch only: a byte copy)     */
+} moe_dtype;
+
+/* Library ABI version (this header: 1). */
+int moe_version(void);
+
+/* Static text for a status code. */
+const char *moe_status_string(int status);
+
+/* The CUDA error code behind the last MOE_ECUDA returned on this host
+ * thread (0 if none). */
+int moe_last_cuda_error(void);
+
+/* Device-side error bits of the kernels, OR-ed since the last call, which
+ * clears them.  Kernels never fault on bad data: they skip the offending row
+ * and set a bit instead.
+ *   bit 0  dispatch: a bounded wait for a staged row ran out of time (the
+ *          kernel stopped early; its output is incomplete)
+ *   bit 1  dispatch: a map entry pointed outside the source or destination
+ *          buffer (that row was not copied)
+ *   bit 2  combine: a map entry pointed outside y, or a group row's source
+ *          entry outside topk_w (that term was dropped)
+ * flags: HOST pointer to one uint32.  Synchronous: waits for the device. */
+int moe_device_errors(uint32_t *flags);
+
+/* ------------------------------------------------------------------------
+ * Plan  [mori #448: StdMoE note (packed_cnt, packed_src, i64 slot map with
+ * -1) and routing-handle note (local_expert_count)].
+ *
+ *   cnt[e]        = number of entries (s,k) with topk_idx[s,k] == e
+ *   off[e]        = sum of cnt[e'] for e' < e; off[E] = valid entries
+ *   tok_map[s,k]  = off[e] + (number of entries before (s,k) in (token, k)
+ *                   order that chose the same expert), or -1 when topk_idx
+ *                   [s,k] is outside [0, E)
+ *   packed_src[r] = s*K + k of the entry whose packed row is r, r < off[E]
+ *   n_invalid[0]  = number of entries outside [0, E)
+ *
+ * Slots are handed out in (token, k) order, so the result is a pure function
+ * of topk_idx (the pages allocate slots with atomics; this library does not).
+ *
+ * topk_idx   int32 [S, K]            device, read
+ * cnt        int32 [E]               device, written
+ * off        int64 [E + 1]           device, written
+ * packed_src int32 [S * K]           device, first off[E] entries written
+ * tok_map    int64 [S, K]            device, written
+ * n_invalid  int32 [1]               device, written
+ * workspace  moe_plan_workspace_size(S, K, E) bytes of device scratch,
+ *            256-byte aligned (NULL allowed when that size is 0); contents
+ *            need no initialisation and are dead after the call.
+ * Limits: S*K < 2^31, 1 <= K <= 32, 1 <= E <= 1024.
+ * ---------------------------------------------------------------------- */
+size_t moe_plan_workspace_size(int64_t S, int K, int E);
+
+int moe_plan(const int32_t *topk_idx, int64_t S, int K, int E,
+             int32_t *cnt, int64_t *off, int32_t *packed_src, int64_t *tok_map,
+             int32_t *n_invalid, void *workspace, size_t workspace_bytes,
+             moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Dedup plan  [mori #448: PR description (ballot dedup: one copy of a token
+ * per destination) and StdMoE note (the receiver's i64 map holds -1 for the
+ * token's experts that live elsewhere)].  Virtual group of expert e is
+ * e / group_size; G = E / group_size groups.
+ *
+ * Entry (s,k) represents group g when topk_idx[s,k] is valid, lies in g, and
+ * no earlier k' of token s lies in g.  Group rows are ordered by group, then
+ * by token.
+ *   gcnt[g]          = group rows of group g;  goff = exclusive prefix sum,
+ *                      goff[G] = R, the number of group rows
+ *   gtok_map[s,k]    = group row of (s,k) if it represents its group, else -1
+ *   grp_src[r]       = s*K + k of the representative of group row r
+ *   grp_tok_map[r,k] = tok_map[s,k] when expert (s,k) belongs to the group of
+ *                      row r, else -1   (s = grp_src[r] / K)
+ *
+ * tok_map      int64 [S, K]  from moe_plan on the same topk_idx
+ * gcnt         int32 [G]; goff int64 [G + 1]; gtok_map int64 [S, K]
+ * grp_src      int32 [S * min(K, G)]        first R entries written
+ * grp_tok_map  int64 [S * min(K, G), K]     first R rows written
+ * Limits: as moe_plan; group_size >= 1 divides E.
+ * ---------------------------------------------------------------------- */
+size_t moe_group_plan_workspace_size(int64_t S, int K, int E, int group_size);
+
+int moe_group_plan(const int32_t *topk_idx, const int64_t *tok_map, int64_t S, int K,
+                   int E, int group_size, int32_t *gcnt, int64_t *goff,
+                   int64_t *gtok_map, int32_t *grp_src, int64_t *grp_tok_map,
+                   void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Dispatch  [mori #448: PR description (16-byte scatter of each token row),
+ * StdMoE note (packed_x[expert, slot]), scale_dim note (scale rows travel
+ * verbatim)].
+ *
+ *   packed_x[tok_map[s,k], :] = x[s, :]          for every tok_map[s,k] >= 0
+ *   packed_scales[tok_map[s,k], :] = x_scales[s, :]   (when n_scales > 0)
+ * Rows of packed_x that no entry maps to are left untouched.
+ *
+ * x             [S, H] of `dtype` (a byte copy: any dtype of that size)
+ * tok_map       int64 [S, K] from moe_plan; entries must be -1 or below S*K
+ * packed_x      [>= off[E], H] of `dtype`; S*K rows always suffice
+ * x_scales      f32 [S, n_scales] or NULL when n_scales == 0
+ * packed_scales f32 [>= off[E], n_scales] or NULL when n_scales == 0
+ * Alignment: x, packed_x, x_scales, packed_scales 16-byte aligned; H*size
+ * and n_scales*4 multiples of 16 (else MOE_EALIGN).
+ * ---------------------------------------------------------------------- */
+int moe_dispatch(const void *x, int64_t S, int64_t H, int dtype, int K,
+                 const int64_t *tok_map, void *packed_x, const float *x_scales,
+                 int64_t n_scales, float *packed_scales, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Dedup dispatch  [mori #448: ballot-dedup send, then convert_dispatch_output
+ * per (received token, k)].  Two stages on `stream`:
+ *   grp_x[r, :]                = x[grp_src[r] / K, :]          r < R = goff[G]
+ *   packed_x[grp_tok_map[r,k]] = grp_x[r, :]      for grp_tok_map[r,k] >= 0
+ * max_rows: rows allocated for grp_x (and grp_src/grp_tok_map); must be at
+ * least S * min(K, G), which bounds R.  Alignment as moe_dispatch.
+ * ---------------------------------------------------------------------- */
+int moe_dispatch_dedup(const void *x, int64_t S, int64_t H, int dtype, int K, int G,
+                       const int64_t *goff, const int32_t *grp_src,
+                       const int64_t *grp_tok_map, int64_t max_rows, void *grp_x,
+                       void *packed_x, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Combine  [mori #448: PR description (gather each token's k expert outputs,
+ * reduce in f32), StdMoE note (sum_k wts[k]*packed_x[slot_k]), accumulator
+ * note (bf16/f32 widened to f32); mori EPv2 combine note (16-byte load-first
+ * gather, whole vector steps per warp)].
+ *
+ *   out[s, j] = round_out( sum over k = 0..K-1 with tok_map[s,k] >= 0 of
+ *                          topk_w[s,k] * y[tok_map[s,k], j] )
+ * The sum is taken in f32 in increasing k, each product and each sum rounded
+ * separately (no fused multiply-add); bf16 output rounds to nearest even.
+ *
+ * y       [>= off[E], H] of in_dtype (MOE_BF16 or MOE_F32)
+ * topk_w  f32 [S, K]; tok_map int64 [S, K] from moe_plan
+ * out     [S, H] of out_dtype (MOE_BF16 or MOE_F32)
+ * Alignment: y, out 16-byte aligned; H a multiple of 8.
+ * ---------------------------------------------------------------------- */
+int moe_combine(const void *y, int in_dtype, const float *topk_w, const int64_t *tok_map,
+                int64_t S, int64_t H, int K, void *out, int out_dtype,
+                moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Dedup combine  [mori #448 StdMoE note: convert_combine_input per received
+ * token, then the gather combine sums over destinations].  Two stages:
+ *   gtok[r, j] = sum over k with grp_tok_map[r,k] >= 0 of
+ *                topk_w[s,k] * y[grp_tok_map[r,k], j]     (f32, s = grp_src[r]/K)
+ *   out[s, j]  = round_out( sum over k with gtok_map[s,k] >= 0 of
+ *                           gtok[gtok_map[s,k], j] )      (f32, unweighted)
+ * gtok: f32 [max_rows, H] device scratch written by the first stage (it is
+ * also the per-group result and may be read afterwards).
+ * max_rows >= S * min(K, G).  Alignment as moe_combine.
+ * ---------------------------------------------------------------------- */
+int moe_combine_dedup(const void *y, int in_dtype, const float *topk_w,
+                      const int64_t *goff, int G, const int32_t *grp_src,
+                      const int64_t *grp_tok_map, const int64_t *gtok_map, int64_t S,
+                      int64_t H, int K, int64_t max_rows, float *gtok, void *out,
+                      int out_dtype, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_PLAN_H */

@@ -5,14 +5,17 @@ tests then compile copies of oracle.c with one plausible mistake planted each
 (a dropped term, a wrong index, a flipped sign, a reversed order, a wrong
 bias...) and check that some pin fails for every one of them.
 """
+import json
 import os
 import subprocess
-import tempfile
+import sys
 
 import pytest
 
 import oracle
 from tests import pins
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 @pytest.mark.parametrize("pin", pins.ALL_PINS, ids=lambda f: f.__name__)
@@ -26,8 +29,9 @@ MUTANTS = [
      [pins.pin_plan_hand_example, pins.pin_plan_bruteforce]),
     ("plan_scan_inclusive", "off[e + 1] = off[e] + cnt[e];", "off[e + 1] = off[e] + cnt[e] + (e == 0);",
      [pins.pin_plan_hand_example, pins.pin_plan_bruteforce]),
-    ("plan_accepts_E", "if (e >= 0 && e < E) {\n                int64_t row",
-     "if (e >= 0 && e <= E) {\n                int64_t row", [pins.pin_plan_bruteforce]),
+    ("plan_invalid_not_marked", "tok_map[i] = -1;\n            }\n        }\n    }\n    free(cursor);\n    *n_invalid",
+     "tok_map[i] = 0;\n            }\n        }\n    }\n    free(cursor);\n    *n_invalid",
+     [pins.pin_plan_hand_example, pins.pin_plan_bruteforce]),
     ("plan_reverse_tokens", "for (int64_t s = 0; s < S; ++s) {\n        for (int k = 0; k < K; ++k) {\n            int64_t i = s * K + k;\n            int32_t e",
      "for (int64_t s = S - 1; s >= 0; --s) {\n        for (int k = 0; k < K; ++k) {\n            int64_t i = s * K + k;\n            int32_t e",
      [pins.pin_plan_hand_example, pins.pin_plan_bruteforce]),
@@ -81,11 +85,22 @@ def test_mutant_is_caught(name, old, new, catchers, tmp_path):
     csrc.write_text(mutated)
     so = tmp_path / "libmutant.so"
     oracle.build(str(csrc), str(so))
-    lib = oracle.load(str(so))
-    caught = []
-    for pin in catchers:
-        try:
-            pin(lib)
-        except AssertionError:
-            caught.append(pin.__name__)
+    # run the pins in a child process so that a mutant which corrupts memory
+    # cannot take the test session down with it
+    script = (
+        "import json, sys\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "import oracle\n"
+        "from tests import pins\n"
+        f"lib = oracle.load({str(so)!r})\n"
+        "caught = []\n"
+        f"for name in {[c.__name__ for c in catchers]!r}:\n"
+        "    try:\n"
+        "        getattr(pins, name)(lib)\n"
+        "    except AssertionError:\n"
+        "        caught.append(name)\n"
+        "print(json.dumps(caught))\n")
+    r = subprocess.run([sys.executable, "-c", script], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, f"mutant {name}: child exited {r.returncode}: {r.stderr[-2000:]}"
+    caught = json.loads(r.stdout.strip().splitlines()[-1])
     assert caught, f"mutant {name} passed every pin it should fail"

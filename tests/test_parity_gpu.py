@@ -1,0 +1,215 @@
+"""GPU path (through the C ABI) against the CPU oracle on the same seeded inputs.
+
+Bar: counts, offsets, maps and dispatched rows bit-exact; combine within
+|gpu - ref| <= 2^-8 |ref| + 1e-6 (one bf16 unit roundoff of the reference
+plus a floor), where ref is the oracle's output.  The kernels add the K
+terms in the oracle's order with separately rounded f32 operations, so the
+combine is also checked for bitwise equality.
+
+Workloads: the pages' shapes (MoonEP S=4096 H=7168 K=8 E=64; Zipf-skewed
+S=8192 E=256; dedup S=4096 H=4096 f32 with 8 groups of 8; fp8 H=6144 E=256 at
+4..1024 tokens; the tiny case), plus ragged, empty and degenerate shapes.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+from tests import gpu_path  # noqa: E402
+from tests.pins import bf16_bits_to_f64  # noqa: E402
+
+TOL_REL = 2.0 ** -8
+TOL_ABS = 1e-6
+
+
+def _as_f64(a: np.ndarray, dt: str) -> np.ndarray:
+    return bf16_bits_to_f64(a) if dt == "bf16" else a.astype(np.float64)
+
+
+def assert_combine_close(got, ref, dt, what="out"):
+    g = _as_f64(got, dt)
+    r = _as_f64(ref, dt)
+    bad = np.abs(g - r) > TOL_REL * np.abs(r) + TOL_ABS
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements outside tolerance, first at " \
+                          f"{np.argwhere(bad)[0]}: gpu {g[bad][0]} ref {r[bad][0]}"
+    # same order of separately rounded f32 operations: identical bits
+    assert np.array_equal(got, ref), f"{what}: within tolerance but not bitwise equal " \
+                                     f"({int((got != ref).sum())} elements differ)"
+
+
+def check_against_oracle(wl, res, ref):
+    for key in ("cnt", "off", "packed_src", "tok_map"):
+        assert np.array_equal(res[key], ref[key]), key
+    assert res["n_invalid"] == ref["n_invalid"]
+    assert np.array_equal(res["packed_x"].view(np.uint8), ref["packed_x"].view(np.uint8))
+    # rows past off[E] keep the poison
+    V = int(ref["off"][-1])
+    assert np.all(res["packed_x_full"][V:].view(np.uint8) == gpu_path.POISON)
+    if "packed_scales" in ref:
+        assert np.array_equal(res["packed_scales"].view(np.uint8),
+                              ref["packed_scales"].view(np.uint8))
+    assert np.array_equal(res["y"].view(np.uint8), ref["y"].view(np.uint8))
+    assert_combine_close(res["out"], ref["out"], wl.out_dtype)
+    if "gcnt" in ref:
+        for key in ("gcnt", "goff", "gtok_map", "grp_src", "grp_tok_map"):
+            assert np.array_equal(res[key], ref[key]), key
+        assert np.array_equal(res["grp_x"].view(np.uint8), ref["grp_x"].view(np.uint8))
+        assert np.array_equal(res["packed_x_dedup"].view(np.uint8),
+                              ref["packed_x_dedup"].view(np.uint8))
+        assert_combine_close(res["gtok"], ref["gtok"], "f32", "gtok")
+        assert_combine_close(res["out_dedup"], ref["out_dedup"], wl.out_dtype, "out_dedup")
+
+
+def run_case(wl):
+    ref = oracle.run_workload(wl)
+    res = gpu_path.run(wl)
+    check_against_oracle(wl, res, ref)
+    return res, ref
+
+
+# ---------------------------------------------------------------------------
+# the pages' workloads at full size
+# ---------------------------------------------------------------------------
+
+@pytest.mark.timeout(600)
+def test_tiny():
+    run_case(workloads.make("tiny", seed=0))
+
+
+@pytest.mark.timeout(600)
+def test_moonep_full_size():
+    """S=4096 H=7168 E=64 K=8 bf16 with per-expert scales: the benchmarked
+    workload, at its full size and launch configuration."""
+    run_case(workloads.make("moonep", seed=0))
+
+
+@pytest.mark.timeout(600)
+def test_zipf_full_size():
+    res, ref = run_case(workloads.make("zipf", seed=0))
+    assert (ref["cnt"] == 0).any() or ref["cnt"].min() < 20   # load imbalance reached
+
+
+@pytest.mark.timeout(600)
+def test_dedup_full_size():
+    run_case(workloads.make("dedup", seed=0))
+
+
+@pytest.mark.timeout(600)
+@pytest.mark.parametrize("S", [0, 1])
+def test_dedup_edge_tokens(S):
+    run_case(workloads.make("dedup", seed=1, S=S))
+
+
+@pytest.mark.timeout(600)
+@pytest.mark.parametrize("S", workloads.FP8_SWEEP_TOKENS)
+def test_fp8_small_token_sweep(S):
+    run_case(workloads.make("fp8small", seed=2, S=S))
+
+
+# ---------------------------------------------------------------------------
+# ragged, degenerate and edge shapes
+# ---------------------------------------------------------------------------
+
+@pytest.mark.timeout(600)
+@pytest.mark.parametrize("S,H,E,K", [
+    (1, 8, 1, 1),          # smallest everything
+    (3, 16, 4, 3),         # K not dividing 32
+    (1023, 64, 8, 8),      # single tile, ragged
+    (1024, 64, 8, 8),      # exactly 8192 entries: largest single-tile plan
+    (1025, 64, 8, 8),      # first two-kernel plan, ragged last tile
+    (2999, 136, 64, 6),    # K = 6, odd row of 17 vectors
+    (777, 24, 1024, 32),   # E = 1024 (largest), K = 32
+    (5000, 256, 37, 5),    # E not a power of two
+    (40000, 16, 256, 8),   # many tiles (320000 entries)
+])
+def test_shapes(S, H, E, K):
+    run_case(workloads.make("moonep", seed=S + H, S=S, H=H, E=E, K=K))
+
+
+@pytest.mark.timeout(600)
+def test_invalid_and_unused_entries():
+    wl = workloads.make("moonep", seed=5, S=2000, H=64, E=32, K=4)
+    idx = wl.topk_idx.copy()
+    idx[::3, 1] = -1
+    idx[::5, 2] = wl.E
+    idx[7, :] = -1          # a token that goes nowhere: its output row is 0
+    idx[::13, 0] = 1 << 30
+    wl.topk_idx = idx
+    res, ref = run_case(wl)
+    assert res["n_invalid"] == int(((idx < 0) | (idx >= wl.E)).sum())
+    assert np.all(res["out"][7] == 0)
+
+
+@pytest.mark.timeout(600)
+def test_repeated_expert_within_token():
+    """Duplicate ids in one token each take their own slot, in k order."""
+    wl = workloads.make("moonep", seed=6, S=500, H=32, E=16, K=4)
+    idx = wl.topk_idx.copy()
+    idx[:, 3] = idx[:, 0]
+    wl.topk_idx = idx
+    run_case(wl)
+
+
+@pytest.mark.timeout(600)
+@pytest.mark.parametrize("gs,K", [(1, 8), (2, 3), (16, 8), (64, 8), (4, 6)])
+def test_dedup_group_sizes(gs, K):
+    wl = workloads.make("dedup", seed=gs * 10 + K, S=700, H=64, K=K)
+    wl.group_size = gs
+    run_case(wl)
+
+
+@pytest.mark.timeout(600)
+def test_f32_output_of_bf16_combine():
+    wl = workloads.make("moonep", seed=8, S=300, H=128)
+    wl.out_dtype = "f32"
+    run_case(wl)
+
+
+# ---------------------------------------------------------------------------
+# properties
+# ---------------------------------------------------------------------------
+
+@pytest.mark.timeout(900)
+def test_bitwise_deterministic_100_launches():
+    """100 launches of each step give the bits of the first (the method of
+    TensorRT-LLM "cluster-scope acquire/release ... MoE GEMM scheduler",
+    determinism check)."""
+    import combine_moe_plan_02_gb300 as moe
+    wl = workloads.make("zipf", seed=3, S=2048, H=1024)
+    d = gpu_path.to_device(wl)
+    p0 = moe.moe_plan(d["topk_idx"], wl.E)
+    px0, _ = moe.moe_dispatch(d["x"], p0.tok_map)
+    o0 = moe.moe_combine(px0, d["topk_w"], p0.tok_map)
+    V = int(p0.off[-1])
+    for _ in range(100):
+        p = moe.moe_plan(d["topk_idx"], wl.E)
+        px, _ = moe.moe_dispatch(d["x"], p.tok_map)
+        o = moe.moe_combine(px, d["topk_w"], p.tok_map)
+        assert torch.equal(p.tok_map, p0.tok_map) and torch.equal(p.off, p0.off)
+        assert torch.equal(p.packed_src[:V], p0.packed_src[:V])
+        assert torch.equal(px[:V].view(torch.int16), px0[:V].view(torch.int16))
+        assert torch.equal(o.view(torch.int16), o0.view(torch.int16))
+
+
+@pytest.mark.timeout(600)
+def test_identity_experts_telescope_at_full_size():
+    """With identity experts the combine returns (sum_k w) * x (mori #448,
+    StdMoE note), checked on the GPU output directly."""
+    wl = workloads.make("tiny", seed=0, S=4096, H=7168, E=64, K=8)
+    res = gpu_path.run(wl)
+    x = bf16_bits_to_f64(wl.x)
+    ref = wl.topk_w.astype(np.float64).sum(axis=1)[:, None] * x
+    got = bf16_bits_to_f64(res["out"])
+    assert np.all(np.abs(got - ref) <= 2 ** -8 * np.abs(ref) + 8 * 2 ** -24 * np.abs(x) * 1.01)
+
+
+@pytest.mark.timeout(600)
+def test_no_device_errors_after_runs():
+    import combine_moe_plan_02_gb300 as moe
+    gpu_path.run(workloads.make("tiny", seed=0))
+    assert moe.moe_device_errors() == 0
