@@ -91,7 +91,7 @@ def test_moonep_full_size():
 @pytest.mark.timeout(600)
 def test_zipf_full_size():
     res, ref = run_case(workloads.make("zipf", seed=0))
-    assert (ref["cnt"] == 0).any() or ref["cnt"].min() < 20   # load imbalance reached
+    assert ref["cnt"].max() > 20 * ref["cnt"].min()   # strong load imbalance reached
 
 
 @pytest.mark.timeout(600)
