@@ -25,6 +25,7 @@ SIGNATURES = {
     "moe_last_cuda_error": (I32, []),
     "moe_plan_workspace_size": (SZ, [I64, I32, I32]),
     "moe_plan": (I32, [P, I64, I32, I32, P, P, P, P, P, P, SZ, P]),
+    "moe_plan_static_scratch": (I32, [P, I64, I32, I32, P, P, P, P, P, P]),
     "moe_group_plan_workspace_size": (SZ, [I64, I32, I32, I32]),
     "moe_group_plan": (I32, [P, P, I64, I32, I32, I32, P, P, P, P, P, P, SZ, P]),
     "moe_dispatch": (I32, [P, I64, I64, I32, I32, P, P, P, I64, P, P]),

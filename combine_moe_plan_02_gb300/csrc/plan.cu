@@ -395,3 +395,84 @@ MOE_EXPORT int moe_group_plan(const int32_t *topk_idx, const int64_t *tok_map, i
     const RankOut o{gcnt, goff, gtok_map, grp_src, nullptr, tok_map, grp_tok_map};
     return run_plan(key, E / group_size, g, o, workspace, workspace_bytes, (cudaStream_t)stream);
 }
+
+// ---------------------------------------------------------------------------
+// moe_plan_static_scratch: moe_plan without a caller-supplied workspace.
+//
+// Some callers cannot hand this library a device workspace: a C or C++ host
+// that links only this library and owns no device allocator, or a process
+// whose device memory belongs to a pool that forbids further cudaMalloc calls
+// (a cudaMalloc may synchronise the device and fragment a packed heap).  For
+// them the tile histograms live in the file-scope array below, which is part
+// of the library image: every GPU that loads the library holds it until the
+// process exits, and this entry point allocates nothing.
+//
+// The array is shared by every call.  Each call overwrites every histogram
+// entry it later reads, so leftover contents from an earlier call need no
+// clearing; but two calls whose plans overlap on the GPU (for example on two
+// streams) race on it and must not be issued.
+// ---------------------------------------------------------------------------
+
+#include <mutex>
+
+// Stated maximum: 256 KiB, enough for the tile histograms of every plan with
+// E <= 511 experts (at most 128 tiles), and of plans with up to 63 tiles at
+// E = 1024.  Larger plans are rejected with MOE_EINVAL.
+#define MOE_STATIC_PLAN_SCRATCH_BYTES (256u * 1024u)
+
+static __device__ __align__(256) unsigned char g_plan_static_scratch[MOE_STATIC_PLAN_SCRATCH_BYTES];
+
+namespace moe {
+namespace {
+
+constexpr size_t kStaticPlanScratchBytes = MOE_STATIC_PLAN_SCRATCH_BYTES;
+constexpr int kMaxStaticDevices = 64;
+std::mutex g_static_scratch_mu;
+void *g_static_scratch_ptr[kMaxStaticDevices];  // device address per device, once known
+
+// Device address of the array on the current device.  In host code the
+// array's name is only a host-side stand-in; the real address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+int static_scratch_address(void **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        set_cuda_error(e);
+        return MOE_ECUDA;
+    }
+    if (dev < 0 || dev >= kMaxStaticDevices) return MOE_EINVAL;
+    std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+    if (g_static_scratch_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_plan_static_scratch);
+        if (e != cudaSuccess || p == nullptr) {
+            set_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+            return MOE_ECUDA;
+        }
+        g_static_scratch_ptr[dev] = p;
+    }
+    *out = g_static_scratch_ptr[dev];
+    return MOE_OK;
+}
+
+} // namespace
+} // namespace moe
+
+MOE_EXPORT int moe_plan_static_scratch(const int32_t *topk_idx, int64_t S, int K, int E,
+                                       int32_t *cnt, int64_t *off, int32_t *packed_src,
+                                       int64_t *tok_map, int32_t *n_invalid,
+                                       moe_stream_t stream)
+{
+    if (int rc = check_plan_args(S, K, E)) return rc;
+    if (!cnt || !off || !n_invalid) return MOE_EINVAL;
+    if (S > 0 && (!topk_idx || !packed_src || !tok_map)) return MOE_EINVAL;
+    const PlanGeom g = plan_geom(S, K);
+    const size_t need = hist_ws_bytes(g, E);
+    if (need > kStaticPlanScratchBytes) return MOE_EINVAL;  // plan too large for the array
+    void *ws = nullptr;
+    if (int rc = static_scratch_address(&ws)) return rc;
+    const DirectKey key{topk_idx, E};
+    const RankOut o{cnt, off, tok_map, packed_src, n_invalid, nullptr, nullptr};
+    return run_plan(key, E, g, o, ws, kStaticPlanScratchBytes, (cudaStream_t)stream);
+}

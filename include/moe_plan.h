@@ -121,6 +121,31 @@ int moe_plan(const int32_t *topk_idx, int64_t S, int K, int E,
              moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Plan without a caller-supplied workspace.  The pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory for
+ * a workspace, such as a C or C++ host linking only this library with no
+ * device allocator of its own, or a process whose device memory belongs to a
+ * pool that forbids further cudaMalloc calls.
+ *
+ * Same arguments, outputs and errors as moe_plan, minus the workspace.  The
+ * tile histograms live in a 256 KiB array inside the library image that
+ * every GPU loading the library holds until the process exits; this call
+ * allocates and frees nothing.  Plans whose moe_plan_workspace_size exceeds
+ * 256 KiB are rejected with MOE_EINVAL (every plan with E <= 511 fits; at
+ * E = 1024, plans of up to 129,024 entries S*K fit).
+ *
+ * The first call on a device (with that device current) looks up the
+ * array's device address once; make that first call before any stream
+ * capture.  All calls share the array and it keeps the last call's contents;
+ * nothing in it needs to start at zero, because each call overwrites every
+ * entry it reads.  Calls that overlap on the GPU (e.g. issued on two
+ * streams, or from two host threads) race on the array: do not overlap them.
+ * ---------------------------------------------------------------------- */
+int moe_plan_static_scratch(const int32_t *topk_idx, int64_t S, int K, int E,
+                            int32_t *cnt, int64_t *off, int32_t *packed_src,
+                            int64_t *tok_map, int32_t *n_invalid, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Dedup plan  [mori #448: PR description (ballot dedup: one copy of a token
  * per destination) and StdMoE note (the receiver's i64 map holds -1 for the
  * token's experts that live elsewhere)].  Virtual group of expert e is

@@ -1,0 +1,89 @@
+"""moe_plan_static_scratch: the plan for callers that cannot allocate a
+device workspace (a host linking only this library with no device allocator,
+or a process whose device memory pool forbids further cudaMalloc calls).
+
+It is called here through the C ABI (ctypes, no Python wrapper) and checked
+against moe_plan, which takes a caller-allocated workspace, on two calls in a
+row: the plan is integer work, so the tolerance is exact equality.  The
+second call uses different routing and a different shape, so leftover
+histograms from the first call cannot pass as correct.  This file is named
+to be collected last.
+"""
+import numpy as np
+import pytest
+
+import workloads
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+
+def _plan_buffers(S, K, E, dev):
+    return (torch.full((E,), -7, dtype=torch.int32, device=dev),
+            torch.full((E + 1,), -7, dtype=torch.int64, device=dev),
+            torch.full((max(S * K, 1),), -7, dtype=torch.int32, device=dev),
+            torch.full((S, K), -7, dtype=torch.int64, device=dev),
+            torch.full((1,), -7, dtype=torch.int32, device=dev))
+
+
+def _static_plan(L, idx, E):
+    S, K = idx.shape
+    cnt, off, src, tmap, ninv = _plan_buffers(S, K, E, idx.device)
+    rc = L.moe_plan_static_scratch(idx.data_ptr(), S, K, E, cnt.data_ptr(), off.data_ptr(),
+                                   src.data_ptr(), tmap.data_ptr(), ninv.data_ptr(),
+                                   torch.cuda.current_stream().cuda_stream)
+    return rc, (cnt, off, src, tmap, ninv)
+
+
+@pytest.mark.timeout(300)
+def test_static_scratch_plan_matches_moe_plan_twice():
+    import combine_moe_plan_02_gb300 as moe
+    L = moe.lib()
+    dev = torch.device("cuda", 0)
+    cases = [
+        workloads.make("moonep", seed=11),                  # 32768 entries: 16 tiles
+        workloads.make("zipf", seed=12, S=6000, H=8),      # 48000 entries, skewed, E=256
+    ]
+    for wl in cases:
+        idx = torch.from_numpy(wl.topk_idx).to(dev)
+        assert moe.moe_plan_workspace_size(wl.S, wl.K, wl.E) > 0   # the scratch is used
+        ref = moe.moe_plan(idx, wl.E)
+        rc, got = _static_plan(L, idx, wl.E)
+        assert rc == 0, L.moe_status_string(rc)
+        torch.cuda.synchronize()
+        V = int(ref.off[-1])
+        for a, b in zip(got, (ref.cnt, ref.off, ref.packed_src, ref.tok_map, ref.n_invalid)):
+            if a.numel() == ref.packed_src.numel():
+                a, b = a[:V], b[:V]
+            assert torch.equal(a, b)
+
+
+@pytest.mark.timeout(300)
+def test_static_scratch_single_tile_and_empty():
+    import combine_moe_plan_02_gb300 as moe
+    L = moe.lib()
+    dev = torch.device("cuda", 0)
+    for S in (0, 5, 1024):
+        wl = workloads.make("tiny", seed=S, S=S, H=8, E=8, K=2)
+        idx = torch.from_numpy(np.ascontiguousarray(wl.topk_idx)).to(dev)
+        ref = moe.moe_plan(idx, wl.E)
+        rc, got = _static_plan(L, idx, wl.E)
+        assert rc == 0
+        torch.cuda.synchronize()
+        assert torch.equal(got[0], ref.cnt) and torch.equal(got[1], ref.off)
+        assert torch.equal(got[3], ref.tok_map) and torch.equal(got[4], ref.n_invalid)
+
+
+@pytest.mark.timeout(300)
+def test_static_scratch_rejects_plans_beyond_its_size():
+    import combine_moe_plan_02_gb300 as moe
+    L = moe.lib()
+    dev = torch.device("cuda", 0)
+    S, K, E = 16384, 8, 1024     # 128 tiles x 1025 counters x 4 bytes > 256 KiB
+    assert moe.moe_plan_workspace_size(S, K, E) > 256 * 1024
+    idx = torch.zeros(S, K, dtype=torch.int32, device=dev)
+    rc, got = _static_plan(L, idx, E)
+    assert rc == 1                                       # MOE_EINVAL, nothing launched
+    torch.cuda.synchronize()
+    assert int(got[4].item()) == -7                      # outputs untouched
