@@ -26,6 +26,10 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kKChunk = 8;   // map entries held in registers at a time
+#ifndef MOE_COMBINE_LANE_STEPS
+#define MOE_COMBINE_LANE_STEPS 8
+#endif
+constexpr int kMaxLaneSteps = MOE_COMBINE_LANE_STEPS;  // 8-element steps per lane per unit
 
 enum WMode { kWeightDirect = 0, kWeightViaSrc = 1, kUnweighted = 2 };
 
@@ -139,6 +143,20 @@ __global__ void __launch_bounds__(kThreads, 2) combine_kernel(CombineArgs a)
         }
         const int64_t pbase = (int64_t)sl * 32 * a.R;
         uint8_t *out_row = a.out + i * out_row_bytes;
+#ifdef MOE_COMBINE_PREFETCH
+        // pull the next unit's K row slices into L2 with bulk prefetches, so
+        // that its register loads find them there
+        if (u + W < units && lane < K) {
+            const int64_t in_ = (u + W) / a.slices;
+            const int sn = (int)(u + W - in_ * a.slices);
+            const int64_t rn = __ldg(a.map + in_ * K + lane);
+            const int64_t p0 = (int64_t)sn * 32 * a.R;
+            const int64_t np = min((int64_t)32 * a.R, a.steps - p0);
+            if (rn >= 0 && rn < a.y_rows && np > 0)
+                bulk_prefetch_l2(a.y + rn * in_row_bytes + p0 * kInBytes,
+                                 (uint32_t)(np * kInBytes));
+        }
+#endif
 
         // the trip count is the same for every lane (shuffles below need the
         // whole warp); lanes past the end of the row are predicated off
@@ -203,12 +221,16 @@ int launch_combine(CombineArgs &a, int in_dt, int out_dt, int wm, cudaStream_t s
 {
     void (*fn)(CombineArgs) = select_kernel(in_dt, out_dt, wm);
     if (!fn) return MOE_EINVAL;
-    // slices: at most 8 steps per lane per unit, slices of equal size
+    // slices: at most kMaxLaneSteps steps per lane per unit, slices of equal
+    // size; finer units even out the work of the persistent warps
     const int64_t lane_steps = (a.steps + 31) / 32;
-    a.slices = (int)((lane_steps + 7) / 8);
+    a.slices = (int)((lane_steps + kMaxLaneSteps - 1) / kMaxLaneSteps);
     a.R = (int)((lane_steps + a.slices - 1) / a.slices);
+    // one cache per (input, output, weight-mode) kernel
+    static KernelCache caches[2][2][3];
+    KernelCache &cache = caches[in_dt == MOE_F32][out_dt == MOE_F32][wm];
     int per_sm = 0;
-    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, 0);
+    cudaError_t err = prepare_kernel(fn, 0, kThreads, cache, &per_sm);
     if (err != cudaSuccess || per_sm < 1) {
         set_cuda_error(err != cudaSuccess ? err : cudaErrorInvalidConfiguration);
         return MOE_ECUDA;

@@ -45,12 +45,53 @@ enum : uint32_t {
     kErrDispatchTimeout = 1u,  // a bounded wait for a staged row ran out of time
     kErrDispatchIndex = 2u,    // dispatch met a row index outside its buffers
     kErrCombineIndex = 4u,     // combine met a row index outside its buffers
+    kErrCombineTimeout = 8u,   // a bounded wait for staged rows in combine ran out of time
 };
 cudaError_t read_dispatch_errors(uint32_t *flags);
 cudaError_t read_combine_errors(uint32_t *flags);
 
 // Number of SMs of the current device (cached per device ordinal).
 int sm_count();
+
+// Per-device launch facts of one kernel, filled on first use.  Raising a
+// kernel's dynamic shared-memory limit can wait for the device, so it is done
+// once per device and size, never per launch; the occupancy query is cached
+// by size too.  Races between host threads only repeat a query.
+constexpr int kMaxCachedDevices = 64;
+struct KernelCache {
+    int smem_limit[kMaxCachedDevices];  // dynamic smem limit already set
+    int occ_smem[kMaxCachedDevices];    // smem of the cached occupancy + 1 (0 = none)
+    int occ[kMaxCachedDevices];         // resident CTAs per SM at occ_smem - 1
+};
+
+// Makes `fn` launchable with `smem` bytes of dynamic shared memory and, if
+// per_sm is given, returns its resident CTAs per SM at that size.
+template <typename F>
+cudaError_t prepare_kernel(F fn, size_t smem, int threads, KernelCache &kc, int *per_sm)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool cached = dev >= 0 && dev < kMaxCachedDevices;
+    if (smem > 48 * 1024 && (!cached || kc.smem_limit[dev] < (int)smem)) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        if (cached) kc.smem_limit[dev] = (int)smem;
+    }
+    if (per_sm) {
+        if (cached && kc.occ_smem[dev] == (int)smem + 1) {
+            *per_sm = kc.occ[dev];
+        } else {
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, fn, threads, smem);
+            if (e != cudaSuccess) return e;
+            if (cached) {
+                kc.occ[dev] = *per_sm;
+                kc.occ_smem[dev] = (int)smem + 1;
+            }
+        }
+    }
+    return cudaSuccess;
+}
 
 // Launch with programmatic dependent launch allowed: the kernel may start
 // while its predecessor in the stream is finishing, and must execute
@@ -158,6 +199,12 @@ __device__ __forceinline__ void bulk_s2g(void *gmem_dst, const void *smem_src, u
 }
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Bulk prefetch of [p, p + bytes) into L2 (no completion to wait for).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 // Wait until at most N of this thread's bulk groups still read shared memory.
 template <int N>

@@ -23,9 +23,18 @@
 namespace moe {
 namespace {
 
-constexpr int kWarpsPerCta = 4;
-constexpr int kStages = 4;
-constexpr int kMaxChunk = 4096;        // bytes of a row moved per stage
+#ifndef MOE_DISPATCH_WARPS
+#define MOE_DISPATCH_WARPS 4
+#endif
+#ifndef MOE_DISPATCH_STAGES
+#define MOE_DISPATCH_STAGES 4
+#endif
+#ifndef MOE_DISPATCH_CHUNK
+#define MOE_DISPATCH_CHUNK 4096
+#endif
+constexpr int kWarpsPerCta = MOE_DISPATCH_WARPS;
+constexpr int kStages = MOE_DISPATCH_STAGES;
+constexpr int kMaxChunk = MOE_DISPATCH_CHUNK;  // bytes of a row moved per stage
 constexpr int kMaxScaleBytes = 1024;   // scale row bytes that travel with a row
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per mbarrier wait
 
@@ -211,22 +220,9 @@ int launch_copy(CopyArgs &a, cudaStream_t stream)
 {
     a.stage_bytes = (a.chunk + a.scale_bytes + 127) / 128 * 128;
     const size_t smem = (size_t)kWarpsPerCta * kStages * a.stage_bytes;
-    static thread_local int configured_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaError_t err = cudaSuccess;
-    if (configured_dev != dev) {
-        err = cudaFuncSetAttribute(dispatch_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   227 * 1024 - (int)sizeof(uint64_t) * kWarpsPerCta * kStages);
-        if (err != cudaSuccess) {
-            set_cuda_error(err);
-            return MOE_ECUDA;
-        }
-        configured_dev = dev;
-    }
+    static KernelCache cache;
     int per_sm = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_bulk_kernel,
-                                                        kWarpsPerCta * 32, smem);
+    cudaError_t err = prepare_kernel(dispatch_bulk_kernel, smem, kWarpsPerCta * 32, cache, &per_sm);
     if (err != cudaSuccess || per_sm < 1) {
         set_cuda_error(err != cudaSuccess ? err : cudaErrorInvalidConfiguration);
         return MOE_ECUDA;

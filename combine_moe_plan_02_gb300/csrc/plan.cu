@@ -13,18 +13,22 @@
 //   the flat entry list i = s*K + k is cut into T tiles of `tile` entries;
 //   a tile is cut into 32 warp sub-tiles of `sub` entries, walked in chunks
 //   of 32 consecutive entries (one per lane).
-//   kernel 1 (only when T > 1): per-tile key histograms -> workspace
+//   kernel 1 (large plans only): per-tile key histograms -> workspace
 //     [T][nkeys + 1] (last column: invalid entries).
 //   kernel 2, one CTA per tile:
 //     (a) per-warp key counts: lanes holding the same key find each other
 //         with __match_any_sync and the lowest lane adds the group size;
-//     (b) programmatic-dependent-launch wait, then the tile histograms give
-//         the global counts and the counts of earlier tiles;
+//     (b) the global counts and the counts of earlier tiles: from (a) when
+//         there is one tile (up to 1024 entries); else, for plans of up to
+//         128K entries, every CTA counts all entries itself (shared-memory
+//         atomics over 16-byte loads; the redundant pass costs less than a
+//         second launch, and for the direct plan it also yields the per-warp
+//         counts of (a)); else after a programmatic-dependent-launch wait,
+//         from kernel 1's tile histograms;
 //     (c) a block scan over keys gives off[];
-//     (d) a scan over the 32 warps per key gives each warp's base;
+//     (d) a shuffle scan over the 32 warps per key gives each warp's base;
 //     (e) the warps walk their chunks again: rank = warp base + running
 //         count + popc(match mask & lanemask_lt).
-//   With T == 1 kernel 2 runs alone and takes the counts from (a).
 // The group plan (dedup) runs the same two kernels on the key "group of
 // the entry, if it is its token's first entry in that group".
 
@@ -35,14 +39,29 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
-constexpr int64_t kSingleTileMax = 8192;   // entries handled by one CTA alone
+constexpr int64_t kSingleTileMax = 1024;   // entries handled by one CTA alone
+#ifndef MOE_PLAN_FUSED_MAX
+#define MOE_PLAN_FUSED_MAX 131072
+#endif
+#ifndef MOE_PLAN_TWO_KERNEL_MIN_TILE
+#define MOE_PLAN_TWO_KERNEL_MIN_TILE 2048
+#endif
+constexpr int64_t kFusedMax = MOE_PLAN_FUSED_MAX;  // entries every CTA can count by itself
 constexpr int64_t kMaxTiles = 128;
+
+// How the counts reach each tile:
+//   kModeSingle    one tile: its own per-warp counts are the global counts;
+//   kModeFused     every tile's CTA counts all n entries itself (one launch,
+//                  no workspace; n <= kFusedMax keeps that redundant pass short);
+//   kModeTwoKernel a histogram kernel writes per-tile counts to the workspace.
+enum PlanMode { kModeSingle = 0, kModeFused = 1, kModeTwoKernel = 2 };
 
 struct PlanGeom {
     int64_t n;      // entries S*K
     int64_t tile;   // entries per tile (multiple of kThreads)
     int64_t sub;    // entries per warp sub-tile (multiple of 32)
     int T;          // tiles
+    int mode;       // PlanMode
 };
 
 PlanGeom plan_geom(int64_t S, int K)
@@ -53,10 +72,16 @@ PlanGeom plan_geom(int64_t S, int K)
     if (g.n <= kSingleTileMax) {
         tile = (g.n + kThreads - 1) / kThreads * kThreads;
         if (tile == 0) tile = kThreads;
+        g.mode = kModeSingle;
     } else {
-        int64_t want = (g.n + kMaxTiles - 1) / kMaxTiles;
+        const int64_t want = (g.n + kMaxTiles - 1) / kMaxTiles;
         tile = (want + kThreads - 1) / kThreads * kThreads;
-        if (tile < 2 * kThreads) tile = 2 * kThreads;
+        if (g.n <= kFusedMax) {
+            g.mode = kModeFused;
+        } else {
+            if (tile < MOE_PLAN_TWO_KERNEL_MIN_TILE) tile = MOE_PLAN_TWO_KERNEL_MIN_TILE;
+            g.mode = kModeTwoKernel;
+        }
     }
     g.tile = tile;
     g.sub = tile / kWarps;
@@ -67,7 +92,7 @@ PlanGeom plan_geom(int64_t S, int K)
 
 size_t hist_ws_bytes(const PlanGeom &g, int nkeys)
 {
-    if (g.T <= 1) return 0;
+    if (g.mode != kModeTwoKernel) return 0;
     size_t b = (size_t)g.T * (size_t)(nkeys + 1) * sizeof(int32_t);
     return (b + 255) / 256 * 256;
 }
@@ -96,6 +121,80 @@ struct DirectKey {
         return (e >= 0 && e < E) ? e : -1;
     }
     __device__ __forceinline__ void emit(int64_t, int64_t, int, const RankOut &) const {}
+
+    static constexpr bool kMergesWarpCounts = true;
+
+    // One entry of the all-entries pass: before this tile -> s_bef, else
+    // s_aft; inside this tile also the count of its warp sub-tile (wc row).
+    __device__ __forceinline__ void add(int e, bool before, int32_t *wc, int32_t *s_aft,
+                                        int32_t *s_bef, int &invalid) const
+    {
+        if (e >= 0 && e < E) {
+            atomicAdd(before ? &s_bef[e] : &s_aft[e], 1);
+            if (wc) atomicAdd(&wc[e], 1);
+        } else {
+            ++invalid;
+        }
+    }
+
+    // Counts all n entries: those before `tile_begin` (a multiple of 1024)
+    // into s_bef, the others into s_aft, and those of this tile [tile_begin,
+    // tile_end) also into their warp sub-tile's row of s_wc.  Returns this
+    // thread's invalid entries.  Each thread takes 16-byte groups of 4
+    // entries (always inside one sub-tile), four groups in flight.
+    __device__ __forceinline__ int count_all(int64_t n, int64_t tile_begin, int64_t tile_end,
+                                             int64_t sub, int wstride, int32_t *s_aft,
+                                             int32_t *s_bef, int32_t *s_wc) const
+    {
+        auto wc_row = [&](int64_t j) -> int32_t * {
+            return (j >= tile_begin && j < tile_end) ? s_wc + ((j - tile_begin) / sub) * wstride
+                                                     : nullptr;
+        };
+        int invalid = 0;
+        int64_t done = 0;
+#ifdef MOE_PLAN_COUNT_MATCH
+        // warp-aggregated: lanes holding the same expert add once
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        for (int64_t c = (int64_t)warp * 32; c < n; c += (int64_t)kWarps * 32) {
+            const int64_t i = c + lane;
+            int e = i < n ? __ldg(idx + i) : -1;
+            const bool valid = e >= 0 && e < E;
+            if (!valid && i < n) ++invalid;
+            const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1 - lane);
+            if (valid && lane == __ffs(peers) - 1) {
+                atomicAdd(c < tile_begin ? &s_bef[e] : &s_aft[e], __popc(peers));
+                if (int32_t *wc = wc_row(c)) atomicAdd(&wc[e], __popc(peers));
+            }
+        }
+        return invalid;
+#endif
+        if ((reinterpret_cast<uintptr_t>(idx) & 15u) == 0) {
+            const int4 *p = reinterpret_cast<const int4 *>(idx);
+            const int64_t n4 = n / 4;
+            for (int64_t q0 = threadIdx.x; q0 < n4; q0 += 4 * kThreads) {
+                int4 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (q0 + u * kThreads < n4) v[u] = __ldg(p + q0 + u * kThreads);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t q = q0 + u * kThreads;
+                    if (q < n4) {
+                        const bool before = q * 4 < tile_begin;
+                        int32_t *wc = wc_row(q * 4);
+                        add(v[u].x, before, wc, s_aft, s_bef, invalid);
+                        add(v[u].y, before, wc, s_aft, s_bef, invalid);
+                        add(v[u].z, before, wc, s_aft, s_bef, invalid);
+                        add(v[u].w, before, wc, s_aft, s_bef, invalid);
+                    }
+                }
+            }
+            done = n4 * 4;
+        }
+        for (int64_t j = done + threadIdx.x; j < n; j += kThreads)
+            add(__ldg(idx + j), j < tile_begin, wc_row(j), s_aft, s_bef, invalid);
+        return invalid;
+    }
 };
 
 struct GroupKey {
@@ -132,6 +231,27 @@ struct GroupKey {
         const int64_t s0 = i - i % K;
         for (int kk = 0; kk < K; ++kk)
             o.grp_tok_map[row * K + kk] = (group(s0 + kk) == g) ? o.tok_map[s0 + kk] : -1;
+    }
+
+    static constexpr bool kMergesWarpCounts = false;
+
+    // Counts the representatives among all n entries (warp chunks of 32, so
+    // that the ballot dedup sees whole tokens); chunks lie wholly before or
+    // wholly after `tile_begin`, a multiple of 1024.  Per-warp counts of the
+    // own tile come from step (a) instead.
+    __device__ __forceinline__ int count_all(int64_t n, int64_t tile_begin, int64_t, int64_t,
+                                             int, int32_t *s_tot, int32_t *s_bef, int32_t *) const
+    {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        for (int64_t c = (int64_t)warp * 32; c < n; c += (int64_t)kWarps * 32) {
+            const int64_t i = c + lane;
+            const int k = chunk_key(i, i < n);
+            const unsigned peers = __match_any_sync(0xffffffffu, k);
+            if (k >= 0 && lane == __ffs(peers) - 1) {
+                atomicAdd(c < tile_begin ? &s_bef[k] : &s_tot[k], __popc(peers));
+            }
+        }
+        return 0;
     }
 };
 
@@ -199,8 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1) plan_rank_kernel(Key key, int nke
                                                              RankOut o)
 {
     extern __shared__ int32_t smem[];
-    int32_t *s_wc = smem;                               // [kWarps][nkeys]
-    int64_t *s_base = reinterpret_cast<int64_t *>(s_wc + ((kWarps * nkeys + 1) & ~1));  // [nkeys]
+    // per-warp counts, rows of odd stride so that the column walk of (d)
+    // (lane l reads row l) touches 32 different banks
+    const int wstride = nkeys | 1;
+    int32_t *s_wc = smem;                               // [kWarps][wstride]
+    int64_t *s_base = reinterpret_cast<int64_t *>(s_wc + ((kWarps * wstride + 1) & ~1));  // [nkeys]
     int32_t *s_tot = reinterpret_cast<int32_t *>(s_base + nkeys);                     // [nkeys]
     int32_t *s_bef = s_tot + nkeys;                                                   // [nkeys]
     __shared__ int64_t s_scan[kWarps];
@@ -208,32 +331,42 @@ __global__ void __launch_bounds__(kThreads, 1) plan_rank_kernel(Key key, int nke
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = blockIdx.x;
-    const bool single = (g.T == 1);
+    const bool single = (g.mode == kModeSingle);
 
     griddep_launch_dependents();
-    // With one tile nothing of this plan ran before: wait for whatever wrote
-    // topk_idx.  With several, kernel 1 was launched without the attribute,
-    // so it (and this kernel) began only after earlier stream work finished.
-    if (single) griddep_wait();
+    // Unless kernel 1 ran first, nothing of this plan ran before: wait for
+    // whatever wrote topk_idx.  In two-kernel mode kernel 1 was launched
+    // without the attribute, so it (and this kernel) began only after earlier
+    // stream work finished, and topk_idx may be read before the wait.
+    if (g.mode != kModeTwoKernel) griddep_wait();
 
-    for (int i = threadIdx.x; i < kWarps * nkeys; i += kThreads) s_wc[i] = 0;
+    for (int i = threadIdx.x; i < kWarps * wstride; i += kThreads) s_wc[i] = 0;
     for (int i = threadIdx.x; i < nkeys; i += kThreads) s_tot[i] = s_bef[i] = 0;
     if (threadIdx.x == 0) s_inval = 0;
     __syncthreads();
 
     const int64_t wbegin = (int64_t)t * g.tile + (int64_t)warp * g.sub;
     const int64_t wend = min(wbegin + g.sub, g.n);
-    int32_t *my_wc = s_wc + warp * nkeys;
+    int32_t *my_wc = s_wc + warp * wstride;
+
+    // keys of the warp's first chunk, fetched now so that their latency
+    // overlaps the counting; (a) and (e) reuse them
+    const int k_first = key.chunk_key(wbegin + lane, wbegin + lane < wend);
+    // in the one-launch mode the direct plan takes the per-warp counts of
+    // its own tile from the all-entries pass in (b)
+    const bool merged = g.mode == kModeFused && Key::kMergesWarpCounts;
 
     // (a) per-warp counts
     int invalid = 0;
-    for (int64_t c = wbegin; c < wend; c += 32) {
-        const int64_t i = c + lane;
-        const int k = key.chunk_key(i, i < wend);
-        if (k == -1) ++invalid;
-        const unsigned peers = __match_any_sync(0xffffffffu, k);
-        if (k >= 0 && lane == __ffs(peers) - 1) my_wc[k] += __popc(peers);
-        __syncwarp();
+    if (!merged) {
+        for (int64_t c = wbegin; c < wend; c += 32) {
+            const int64_t i = c + lane;
+            const int k = (c == wbegin) ? k_first : key.chunk_key(i, i < wend);
+            if (k == -1) ++invalid;
+            const unsigned peers = __match_any_sync(0xffffffffu, k);
+            if (k >= 0 && lane == __ffs(peers) - 1) my_wc[k] += __popc(peers);
+            __syncwarp();
+        }
     }
     if (Key::kCountsInvalid && single) {
         for (int sh = 16; sh; sh >>= 1) invalid += __shfl_xor_sync(0xffffffffu, invalid, sh);
@@ -245,9 +378,20 @@ __global__ void __launch_bounds__(kThreads, 1) plan_rank_kernel(Key key, int nke
         __syncthreads();
         for (int e = threadIdx.x; e < nkeys; e += kThreads) {
             int32_t tot = 0;
-            for (int w = 0; w < kWarps; ++w) tot += s_wc[w * nkeys + e];
+            for (int w = 0; w < kWarps; ++w) tot += s_wc[w * wstride + e];
             s_tot[e] = tot;
         }
+    } else if (g.mode == kModeFused) {
+        // s_tot collects the entries from this tile on, s_bef those before
+        const int64_t tile_begin = (int64_t)t * g.tile;
+        int inv = key.count_all(g.n, tile_begin, min(tile_begin + g.tile, g.n), g.sub, wstride,
+                                s_tot, s_bef, s_wc);
+        if (Key::kCountsInvalid && t == 0) {
+            for (int sh = 16; sh; sh >>= 1) inv += __shfl_xor_sync(0xffffffffu, inv, sh);
+            if (lane == 0 && inv) atomicAdd(&s_inval, inv);
+        }
+        __syncthreads();
+        for (int k = threadIdx.x; k < nkeys; k += kThreads) s_tot[k] += s_bef[k];
     } else {
         griddep_wait();  // tile histograms of kernel 1 are complete and visible
         const int stride = nkeys + 1;
@@ -284,21 +428,23 @@ __global__ void __launch_bounds__(kThreads, 1) plan_rank_kernel(Key key, int nke
         if (o.n_invalid) *o.n_invalid = s_inval;
     }
 
-    // (d) exclusive scan over warps, per key, relative to the tile base
-    if (e < nkeys) {
-        int32_t run = 0;
-        for (int w = 0; w < kWarps; ++w) {
-            const int32_t c = s_wc[w * nkeys + e];
-            s_wc[w * nkeys + e] = run;
-            run += c;
+    // (d) exclusive scan over the 32 warps, per key, relative to the tile
+    // base: warp w takes keys w, w+32, ...; lane l holds warp l's count
+    for (int k = warp; k < nkeys; k += kWarps) {
+        const int32_t c = s_wc[lane * wstride + k];
+        int32_t x = c;
+        for (int sh = 1; sh < 32; sh <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, x, sh);
+            if (lane >= sh) x += y;
         }
+        s_wc[lane * wstride + k] = x - c;
     }
     __syncthreads();
 
     // (e) assign ranks
     for (int64_t c = wbegin; c < wend; c += 32) {
         const int64_t i = c + lane;
-        const int k = key.chunk_key(i, i < wend);
+        const int k = (c == wbegin) ? k_first : key.chunk_key(i, i < wend);
         const unsigned peers = __match_any_sync(0xffffffffu, k);
         int64_t row = -1;
         if (k >= 0) row = s_base[k] + my_wc[k] + __popc(peers & lanemask_lt());
@@ -322,16 +468,16 @@ int run_plan(Key key, int nkeys, const PlanGeom &g, const RankOut &o, void *ws,
     const size_t need = hist_ws_bytes(g, nkeys);
     if (need > 0 && (ws == nullptr || ws_bytes < need)) return MOE_EINVAL;
     if (need > 0 && (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOE_EALIGN;
-    if (g.T > 1) {
+    if (g.mode == kModeTwoKernel) {
         const size_t smem1 = (size_t)(nkeys + 1) * sizeof(int32_t);
         plan_hist_kernel<Key><<<g.T, kThreads, smem1, stream>>>(key, nkeys, g,
                                                                  static_cast<int32_t *>(ws));
         if (int rc = check_launch()) return rc;
     }
-    const size_t smem2 = (size_t)((kWarps * nkeys + 1) & ~1) * sizeof(int32_t) +
+    const size_t smem2 = (size_t)((kWarps * (nkeys | 1) + 1) & ~1) * sizeof(int32_t) +
                          (size_t)nkeys * (sizeof(int64_t) + 2 * sizeof(int32_t));
-    cudaError_t err = cudaFuncSetAttribute(plan_rank_kernel<Key>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
+    static KernelCache cache;  // one per Key instantiation
+    cudaError_t err = prepare_kernel(plan_rank_kernel<Key>, smem2, kThreads, cache, nullptr);
     if (err == cudaSuccess)
         err = launch_pdl(plan_rank_kernel<Key>, dim3(g.T), dim3(kThreads), smem2, stream, key,
                          nkeys, g, static_cast<const int32_t *>(ws), o);
@@ -416,8 +562,8 @@ MOE_EXPORT int moe_group_plan(const int32_t *topk_idx, const int64_t *tok_map, i
 #include <mutex>
 
 // Stated maximum: 256 KiB, enough for the tile histograms of every plan with
-// E <= 511 experts (at most 128 tiles), and of plans with up to 63 tiles at
-// E = 1024.  Larger plans are rejected with MOE_EINVAL.
+// E <= 511 experts (at most 128 tiles); plans of up to 131,072 entries use no
+// scratch at all.  Larger plans are rejected with MOE_EINVAL.
 #define MOE_STATIC_PLAN_SCRATCH_BYTES (256u * 1024u)
 
 static __device__ __align__(256) unsigned char g_plan_static_scratch[MOE_STATIC_PLAN_SCRATCH_BYTES];

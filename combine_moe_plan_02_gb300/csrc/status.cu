@@ -9,7 +9,14 @@ constexpr int kMaxDevices = 64;
 int g_sm_count[kMaxDevices];  // 0 = not queried yet
 } // namespace
 
-void set_cuda_error(cudaError_t e) { t_last_cuda_error = (int)e; }
+// Records the error for moe_last_cuda_error() and consumes the runtime's
+// pending copy, so that a failure reported here does not resurface at the
+// caller's next, unrelated CUDA call.
+void set_cuda_error(cudaError_t e)
+{
+    t_last_cuda_error = (int)e;
+    (void)cudaGetLastError();
+}
 
 int sm_count()
 {

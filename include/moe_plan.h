@@ -131,8 +131,8 @@ int moe_plan(const int32_t *topk_idx, int64_t S, int K, int E,
  * tile histograms live in a 256 KiB array inside the library image that
  * every GPU loading the library holds until the process exits; this call
  * allocates and frees nothing.  Plans whose moe_plan_workspace_size exceeds
- * 256 KiB are rejected with MOE_EINVAL (every plan with E <= 511 fits; at
- * E = 1024, plans of up to 129,024 entries S*K fit).
+ * 256 KiB are rejected with MOE_EINVAL (every plan with E <= 511 fits, and
+ * so does every plan of up to 131,072 entries S*K, which needs no scratch).
  *
  * The first call on a device (with that device current) looks up the
  * array's device address once; make that first call before any stream

@@ -36,18 +36,20 @@ def test_version_and_status_strings(L):
 def test_plan_workspace_size(L):
     assert L.moe_plan_workspace_size(128, 2, 8) == 0            # one tile: no scratch
     assert L.moe_plan_workspace_size(1024, 8, 64) == 0          # 8192 entries: one tile
-    ws = L.moe_plan_workspace_size(4096, 8, 64)
+    assert L.moe_plan_workspace_size(4096, 8, 64) == 0          # one launch, no scratch
+    assert L.moe_plan_workspace_size(16384, 8, 64) == 0         # 131072 entries: still one launch
+    ws = L.moe_plan_workspace_size(16385, 8, 64)                # beyond: tile histograms
     assert ws > 0 and ws % 256 == 0
-    assert L.moe_plan_workspace_size(4096, 0, 64) == 0          # invalid K
-    assert L.moe_group_plan_workspace_size(4096, 8, 64, 8) > 0
+    assert L.moe_plan_workspace_size(20000, 0, 64) == 0         # invalid K
+    assert L.moe_group_plan_workspace_size(20000, 8, 64, 8) > 0
     assert L.moe_group_plan_workspace_size(4096, 8, 64, 7) == 0  # 7 does not divide 64
 
 
 @pytest.mark.parametrize("args,want", [
     (dict(S=-1), EINVAL), (dict(K=0), EINVAL), (dict(K=33), EINVAL), (dict(E=0), EINVAL),
     (dict(E=1025), EINVAL), (dict(S=1 << 28, K=8), EINVAL), (dict(cnt=None), EINVAL),
-    (dict(tok_map=None), EINVAL), (dict(ws=None, S=4096, K=8), EINVAL),
-    (dict(ws_bytes=16, S=4096, K=8), EINVAL),
+    (dict(tok_map=None), EINVAL), (dict(ws=None, S=20000, K=8), EINVAL),
+    (dict(ws_bytes=16, S=20000, K=8), EINVAL),
 ])
 def test_plan_rejects(L, args, want):
     a = dict(idx=FAKE, S=16, K=2, E=8, cnt=FAKE, off=FAKE, src=FAKE, tok_map=FAKE, ninv=FAKE,
@@ -58,7 +60,7 @@ def test_plan_rejects(L, args, want):
 
 
 def test_plan_rejects_misaligned_workspace(L):
-    assert L.moe_plan(FAKE, 4096, 8, 64, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 16, 1 << 20,
+    assert L.moe_plan(FAKE, 20000, 8, 64, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 16, 1 << 20,
                       None) == EALIGN
 
 

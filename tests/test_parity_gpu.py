@@ -121,7 +121,9 @@ def test_fp8_small_token_sweep(S):
     (3, 16, 4, 3),         # K not dividing 32
     (1023, 64, 8, 8),      # single tile, ragged
     (1024, 64, 8, 8),      # exactly 8192 entries: largest single-tile plan
-    (1025, 64, 8, 8),      # first two-kernel plan, ragged last tile
+    (1025, 64, 8, 8),      # first multi-tile plan, ragged last tile
+    (16384, 8, 64, 8),     # largest one-launch multi-tile plan (131072 entries)
+    (16385, 8, 64, 8),     # smallest two-kernel plan
     (2999, 136, 64, 6),    # K = 6, odd row of 17 vectors
     (777, 24, 1024, 32),   # E = 1024 (largest), K = 32
     (5000, 256, 37, 5),    # E not a power of two

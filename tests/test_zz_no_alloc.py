@@ -42,8 +42,8 @@ def test_static_scratch_plan_matches_moe_plan_twice():
     L = moe.lib()
     dev = torch.device("cuda", 0)
     cases = [
-        workloads.make("moonep", seed=11),                  # 32768 entries: 16 tiles
-        workloads.make("zipf", seed=12, S=6000, H=8),      # 48000 entries, skewed, E=256
+        workloads.make("moonep", seed=11, S=20000, H=8),    # 160000 entries: 79 tiles
+        workloads.make("zipf", seed=12, S=17000, H=8),      # 136000 entries, skewed, E=256
     ]
     for wl in cases:
         idx = torch.from_numpy(wl.topk_idx).to(dev)
@@ -80,7 +80,7 @@ def test_static_scratch_rejects_plans_beyond_its_size():
     import combine_moe_plan_02_gb300 as moe
     L = moe.lib()
     dev = torch.device("cuda", 0)
-    S, K, E = 16384, 8, 1024     # 128 tiles x 1025 counters x 4 bytes > 256 KiB
+    S, K, E = 32768, 8, 1024     # 128 tiles x 1025 counters x 4 bytes > 256 KiB
     assert moe.moe_plan_workspace_size(S, K, E) > 256 * 1024
     idx = torch.zeros(S, K, dtype=torch.int32, device=dev)
     rc, got = _static_plan(L, idx, E)
