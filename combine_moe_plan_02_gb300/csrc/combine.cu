@@ -27,7 +27,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kKChunk = 8;   // map entries held in registers at a time
 #ifndef MOE_COMBINE_LANE_STEPS
-#define MOE_COMBINE_LANE_STEPS 8
+#define MOE_COMBINE_LANE_STEPS 4
 #endif
 constexpr int kMaxLaneSteps = MOE_COMBINE_LANE_STEPS;  // 8-element steps per lane per unit
 
@@ -143,20 +143,6 @@ __global__ void __launch_bounds__(kThreads, 2) combine_kernel(CombineArgs a)
         }
         const int64_t pbase = (int64_t)sl * 32 * a.R;
         uint8_t *out_row = a.out + i * out_row_bytes;
-#ifdef MOE_COMBINE_PREFETCH
-        // pull the next unit's K row slices into L2 with bulk prefetches, so
-        // that its register loads find them there
-        if (u + W < units && lane < K) {
-            const int64_t in_ = (u + W) / a.slices;
-            const int sn = (int)(u + W - in_ * a.slices);
-            const int64_t rn = __ldg(a.map + in_ * K + lane);
-            const int64_t p0 = (int64_t)sn * 32 * a.R;
-            const int64_t np = min((int64_t)32 * a.R, a.steps - p0);
-            if (rn >= 0 && rn < a.y_rows && np > 0)
-                bulk_prefetch_l2(a.y + rn * in_row_bytes + p0 * kInBytes,
-                                 (uint32_t)(np * kInBytes));
-        }
-#endif
 
         // the trip count is the same for every lane (shuffles below need the
         // whole warp); lanes past the end of the row are predicated off
