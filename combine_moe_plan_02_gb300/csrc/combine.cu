@@ -104,8 +104,11 @@ template <> struct Io<float> {
     }
 };
 
+#ifndef MOE_COMBINE_MIN_BLOCKS
+#define MOE_COMBINE_MIN_BLOCKS 2
+#endif
 template <typename Tin, typename Tout, int WM>
-__global__ void __launch_bounds__(kThreads, 2) combine_kernel(CombineArgs a)
+__global__ void __launch_bounds__(kThreads, MOE_COMBINE_MIN_BLOCKS) combine_kernel(CombineArgs a)
 {
     griddep_wait();  // y, map, weights come from earlier stream work
     griddep_launch_dependents();
@@ -125,14 +128,14 @@ __global__ void __launch_bounds__(kThreads, 2) combine_kernel(CombineArgs a)
         const int64_t i = u / a.slices;
         const int sl = (int)(u - i * a.slices);
         // this lane's map entry and weight (lane k <-> entry k)
-        int64_t my_row = -1;
+        int32_t my_row = -1;  // rows of y are below 2^31 (S*K < 2^31)
         float my_w = 1.0f;
         if (lane < K) {
-            my_row = __ldg(a.map + i * K + lane);
+            const int64_t r = __ldg(a.map + i * K + lane);
+            my_row = (r >= 0 && r < a.y_rows) ? (int32_t)r : (r == -1 ? -1 : -2);
             int64_t wr = i;
             if (WM == kWeightViaSrc) wr = (int64_t)(__ldg(a.wsrc + i) / K);
-            const bool ok = my_row >= -1 && my_row < a.y_rows && (WM != kWeightViaSrc ||
-                                                                 (wr >= 0 && wr < a.w_rows));
+            const bool ok = my_row >= -1 && (WM != kWeightViaSrc || (wr >= 0 && wr < a.w_rows));
             if (!ok) {
                 // never gather outside the buffers: drop the term and report
                 atomicOr(&g_combine_error, kErrCombineIndex);
@@ -156,12 +159,12 @@ __global__ void __launch_bounds__(kThreads, 2) combine_kernel(CombineArgs a)
                 // load first: every gather of this chunk of k is in flight
                 // before the first add
                 uint4 v[kKChunk][Io<Tin>::kVec];
-                int64_t rk[kKChunk];
+                int32_t rk[kKChunk];
 #pragma unroll
                 for (int kk = 0; kk < kKChunk; ++kk) {
                     rk[kk] = __shfl_sync(0xffffffffu, my_row, (k0 + kk) & 31);
                     if (active && k0 + kk < K && rk[kk] >= 0)
-                        Io<Tin>::load(v[kk], a.y + rk[kk] * in_row_bytes, p);
+                        Io<Tin>::load(v[kk], a.y + (int64_t)rk[kk] * in_row_bytes, p);
                 }
 #pragma unroll
                 for (int kk = 0; kk < kKChunk; ++kk) {

@@ -73,7 +73,9 @@ cudaError_t prepare_kernel(F fn, size_t smem, int threads, KernelCache &kc, int 
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const bool cached = dev >= 0 && dev < kMaxCachedDevices;
-    if (smem > 48 * 1024 && (!cached || kc.smem_limit[dev] < (int)smem)) {
+    // set whenever dynamic memory is used: static shared memory counts
+    // against the same 48 KB default
+    if (smem > 0 && (!cached || kc.smem_limit[dev] < (int)smem)) {
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         if (cached) kc.smem_limit[dev] = (int)smem;

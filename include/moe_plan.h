@@ -84,6 +84,8 @@ int moe_last_cuda_error(void);
  *          buffer (that row was not copied)
  *   bit 2  combine: a map entry pointed outside y, or a group row's source
  *          entry outside topk_w (that term was dropped)
+ *   bit 3  combine: a bounded wait for staged rows ran out of time (the
+ *          kernel stopped early; its output is incomplete)
  * flags: HOST pointer to one uint32.  Synchronous: waits for the device. */
 int moe_device_errors(uint32_t *flags);
 
