@@ -86,7 +86,7 @@ CLOCK_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slow
 
 
 class ClockSampler:
-    def __init__(self, device_index: int, interval_ms: int = 50):
+    def __init__(self, device_index: int, interval_ms: int = 100):
         self.proc = None
         self.lines = []
         try:
@@ -236,6 +236,92 @@ def run_reference(args):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+# ---------------------------------------------------------------------------
+# small-token latency (the mori EPv2 latency tables' shape: H=6144, top-8,
+# 4..32 tokens; here on one GPU with fp8 rows and per-128 scales)
+# ---------------------------------------------------------------------------
+
+def small_token_latency(dev, reps: int = 50):
+    """µs per plan + dispatch (fp8 rows + f32 scales) + combine (bf16) call
+    sequence at small token counts, eager and replayed from a CUDA graph."""
+    import torch
+
+    import combine_moe_plan_02_gb300 as moe
+    res = {"workload": "fp8small: H=6144 E=256 K=8, fp8 e4m3 rows + 48 f32 scales per row, "
+                       "bf16 expert outputs, bf16 combine; inputs resident, y precomputed",
+           "S": [], "eager_us": [], "graph_us": [], "plan_us": [], "dispatch_us": [],
+           "combine_us": []}
+    stream = torch.cuda.Stream(dev)  # graphs are captured on a non-default stream
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        _small_token_sweep(moe, torch, dev, stream, reps, res)
+    torch.cuda.synchronize(dev)
+    return res
+
+
+def _small_token_sweep(moe, torch, dev, stream, reps, res):
+    for S in workloads.FP8_SWEEP_TOKENS:
+        wl = workloads.make("fp8small", seed=S, S=S)
+        E, K, H = wl.E, wl.K, wl.H
+        idx = torch.from_numpy(wl.topk_idx).to(dev)
+        w = torch.from_numpy(wl.topk_w).to(dev)
+        x = torch.from_numpy(wl.x).to(dev).view(torch.float8_e4m3fn)
+        xs = torch.from_numpy(wl.x_scales).to(dev)
+        plan = moe.moe_plan(idx, E)
+        px, ps = moe.moe_dispatch(x, plan.tok_map, x_scales=xs)
+        y = (px.float() * ps.repeat_interleave(wl.scale_block, dim=1)).to(torch.bfloat16)
+        out = torch.empty(S, H, dtype=torch.bfloat16, device=dev)
+
+        def calls():
+            moe.moe_plan(idx, E, out=plan, stream=stream)
+            moe.moe_dispatch(x, plan.tok_map, packed_x=px, x_scales=xs, packed_scales=ps,
+                             stream=stream)
+            moe.moe_combine(y, w, plan.tok_map, out=out, stream=stream)
+
+        for _ in range(10):
+            calls()
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps)]
+        for e in ev:
+            e[0].record(stream)
+            moe.moe_plan(idx, E, out=plan, stream=stream)
+            e[1].record(stream)
+            moe.moe_dispatch(x, plan.tok_map, packed_x=px, x_scales=xs, packed_scales=ps,
+                             stream=stream)
+            e[2].record(stream)
+            moe.moe_combine(y, w, plan.tok_map, out=out, stream=stream)
+            e[3].record(stream)
+        torch.cuda.synchronize()
+        step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(reps)]
+        for a, b in step_ev:
+            a.record(stream)
+            calls()
+            b.record(stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            calls()
+        for _ in range(5):
+            g.replay()
+        torch.cuda.synchronize()
+        g_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(reps)]
+        for a, b in g_ev:
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        med = lambda xs_: round(1e3 * statistics.median(xs_), 2)
+        res["S"].append(S)
+        res["eager_us"].append(med([a.elapsed_time(b) for a, b in step_ev]))
+        res["graph_us"].append(med([a.elapsed_time(b) for a, b in g_ev]))
+        res["plan_us"].append(med([e[0].elapsed_time(e[1]) for e in ev]))
+        res["dispatch_us"].append(med([e[1].elapsed_time(e[2]) for e in ev]))
+        res["combine_us"].append(med([e[2].elapsed_time(e[3]) for e in ev]))
+    return res
 
 
 # ---------------------------------------------------------------------------
@@ -415,6 +501,8 @@ def run_ours(args):
         "wall_s_timed": round(wall, 4),
         "clocks": clocks,
     }
+    if rank == 0 and not args.no_small_tokens:
+        line["small_tokens"] = small_token_latency(dev)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
         line["cpu_baseline"]["host_cpus"] = os.cpu_count()
@@ -434,6 +522,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the timed CPU oracle leg (profiling runs)")
+    ap.add_argument("--no-small-tokens", action="store_true",
+                    help="skip the small-token latency sweep (profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
