@@ -501,6 +501,30 @@ def run_ours(args):
         "wall_s_timed": round(wall, 4),
         "clocks": clocks,
     }
+    if rank == 0:
+        # the quantising dispatch on the same batch: bf16 rows in, E4M3 codes
+        # and one f32 scale per 128 elements out (timed alone, L2 flushed)
+        pq = torch.empty(S * K, H, dtype=torch.uint8, device=dev)
+        psc = torch.empty(S * K, H // 128, dtype=torch.float32, device=dev)
+        for _ in range(3):
+            moe.moe_dispatch_quant_fp8(x, plan.tok_map, packed_q=pq, packed_scales=psc,
+                                       stream=stream)
+        qev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for a_, b_ in qev:
+            flush_l2(3)
+            a_.record(stream)
+            moe.moe_dispatch_quant_fp8(x, plan.tok_map, packed_q=pq, packed_scales=psc,
+                                       stream=stream)
+            b_.record(stream)
+        torch.cuda.synchronize()
+        tq = statistics.mean(a_.elapsed_time(b_) for a_, b_ in qev)
+        qbytes = S * H * 2 + S * K * 8 + V * H + V * (H // 128) * 4
+        line["dispatch_quant_fp8"] = {
+            "us": round(1e3 * tq, 2), "GB_per_s": round(qbytes / (tq / 1e3) / 1e9, 1),
+            "frac_of_peak": round(qbytes / (tq / 1e3) / 1e9 / peak, 4),
+            "algorithmic_bytes": qbytes,
+            "what": "bf16 rows -> E4M3 codes + f32 scale per 128 elements, K packed rows each"}
     if rank == 0 and not args.no_small_tokens:
         line["small_tokens"] = small_token_latency(dev)
     if rank == 0 and not args.no_cpu_baseline:

@@ -20,7 +20,8 @@ from . import _abi
 from ._abi import MoeError, MOE_BF16, MOE_F32, MOE_FP8_E4M3  # noqa: F401
 
 __all__ = [
-    "moe_plan", "moe_group_plan", "moe_dispatch", "moe_dispatch_dedup", "moe_combine",
+    "moe_plan", "moe_group_plan", "moe_dispatch", "moe_dispatch_dedup", "moe_dispatch_quant_fp8",
+    "moe_combine",
     "moe_combine_dedup", "moe_plan_workspace_size", "moe_group_plan_workspace_size",
     "moe_device_errors", "Plan", "GroupPlan", "MoeError", "lib",
 ]
@@ -165,6 +166,25 @@ def moe_dispatch(x: torch.Tensor, tok_map: torch.Tensor, *, packed_x: Optional[t
         _ptr(x), S, H, _dt(x), K, _ptr(tok_map), _ptr(packed_x), _ptr(x_scales), n_scales,
         _ptr(packed_scales), _stream(stream)))
     return packed_x, packed_scales
+
+
+def moe_dispatch_quant_fp8(x: torch.Tensor, tok_map: torch.Tensor, *, block: int = 128,
+                           packed_q: Optional[torch.Tensor] = None,
+                           packed_scales: Optional[torch.Tensor] = None, stream=None):
+    """bf16 rows -> blockwise E4M3 codes + f32 scales in the K packed rows of
+    each token.  Returns (packed_q as float8_e4m3fn, packed_scales)."""
+    if x.dtype != torch.bfloat16:
+        raise TypeError("x must be bfloat16")
+    S, H = x.shape
+    K = tok_map.shape[1]
+    if packed_q is None:
+        packed_q = torch.empty(S * K, H, dtype=torch.float8_e4m3fn, device=x.device)
+    if packed_scales is None:
+        packed_scales = torch.empty(S * K, H // block, dtype=torch.float32, device=x.device)
+    _abi.check("moe_dispatch_quant_fp8", lib().moe_dispatch_quant_fp8(
+        _ptr(x), S, H, K, _ptr(tok_map), block, _ptr(packed_q), _ptr(packed_scales),
+        _stream(stream)))
+    return packed_q, packed_scales
 
 
 def moe_dispatch_dedup(x: torch.Tensor, gp: GroupPlan, *, packed_x: Optional[torch.Tensor] = None,

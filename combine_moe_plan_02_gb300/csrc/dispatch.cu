@@ -20,6 +20,8 @@
 
 #include "common.cuh"
 
+#include <cuda_fp8.h>
+
 namespace moe {
 namespace {
 
@@ -200,6 +202,133 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) dispatch_bulk_kernel(CopyAr
     }
 }
 
+// ---------------------------------------------------------------------------
+// Quantising dispatch: bf16 rows in, blockwise E4M3 codes and f32 scales out,
+// each written to the token's K packed rows.  Sources: ROCm/mori "Draft: cco +
+// flydsl dispatch/combine #448", Fp8BlockwiseQuant notes (per-block amax and
+// f32 scale, then the fp8 cast; the coalesced version reduces the block amax
+// across lanes with a butterfly) and scale_dim note (scale rows travel with
+// the token).  The rule: scale = amax / 448 (1 for an all-zero block),
+// code = E4M3(v / scale), both divisions IEEE f32, the cast to nearest even
+// and saturating.
+//
+// A warp owns (token, slice) units: each lane holds 8 consecutive elements
+// (one 16-byte load), a block of `block` elements spans block/8 lanes, and
+// its amax is an xor-shuffle reduction inside that lane group.  All of a
+// unit's loads are issued first.  Each lane then stores its 8 codes (8
+// bytes; a warp writes 256 contiguous bytes) to every destination row, and
+// the first lane of each block stores the block's scale.
+// ---------------------------------------------------------------------------
+
+constexpr int kQThreads = 256;
+constexpr int kQMaxIters = 8;  // 256-element steps per lane group per unit
+
+struct QuantArgs {
+    const uint8_t *x;         // bf16 [S, H]
+    int64_t S, H;
+    int K;
+    const int64_t *tok_map;   // [S, K]
+    int64_t dst_rows;         // rows of the packed buffers (bounds check)
+    int block;                // elements per scale (16..256, power of two)
+    int iters;                // 256-element steps per row
+    int R;                    // steps per unit
+    int slices;               // units per row
+    uint8_t *q;               // [dst_rows, H] E4M3 codes
+    float *scales;            // [dst_rows, H / block]
+};
+
+template <int GL>  // lanes per block (block / 8)
+__global__ void __launch_bounds__(kQThreads, 2) dispatch_quant_kernel(QuantArgs a)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = ((int64_t)blockIdx.x * kQThreads + threadIdx.x) >> 5;
+    const int64_t W = ((int64_t)gridDim.x * kQThreads) >> 5;
+    const int64_t units = a.S * a.slices;
+    const int K = a.K;
+    const int64_t nb = a.H / a.block;
+
+    for (int64_t u = gw; u < units; u += W) {
+        const int64_t s = u / a.slices;
+        const int sl = (int)(u - s * a.slices);
+        int32_t my_row = -1;
+        if (lane < K) {
+            const int64_t r = __ldg(a.tok_map + s * K + lane);
+            if (r >= 0 && r < a.dst_rows) {
+                my_row = (int32_t)r;
+            } else if (r != -1) {
+                atomicOr(&g_dispatch_error, kErrDispatchIndex);
+            }
+        }
+        // load first: every 16-byte load of the unit is in flight
+        uint4 v[kQMaxIters];
+        const int it0 = sl * a.R;
+#pragma unroll
+        for (int r = 0; r < kQMaxIters; ++r) {
+            const int64_t e = ((int64_t)(it0 + r) * 32 + lane) * 8;  // first element
+            if (r < a.R && it0 + r < a.iters && e < a.H)
+                v[r] = ld_stream16(a.x + (s * a.H + e) * 2);
+        }
+#pragma unroll
+        for (int r = 0; r < kQMaxIters; ++r) {
+            if (r >= a.R || it0 + r >= a.iters) break;  // uniform across the warp
+            const int64_t e = ((int64_t)(it0 + r) * 32 + lane) * 8;
+            const bool active = e < a.H;
+            float f[8];
+            const uint32_t w4[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                f[2 * q] = __uint_as_float(w4[q] << 16);
+                f[2 * q + 1] = __uint_as_float(w4[q] & 0xffff0000u);
+            }
+            float amax = 0.0f;
+            if (active) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(f[q]));
+            }
+#pragma unroll
+            for (int o = GL / 2; o > 0; o >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+            // v / scale, correctly rounded, by Markstein's correction step
+            // (P. Markstein, IBM J. Res. Dev. 34(1), 1990): with y = RN(1/scale)
+            // and q = RN(v*y), the residual v - q*scale is exact under FMA and
+            // RN(q + residual*y) = RN(v/scale).  One reciprocal per block
+            // instead of a full division per element.  A zero residual means
+            // q0 is the exact quotient; returning it keeps the sign of -0.
+            const float y = __frcp_rn(scale);
+            auto quot = [&](float v) {
+                const float q0 = __fmul_rn(v, y);
+                const float r = __fmaf_rn(-q0, scale, v);
+                return r == 0.0f ? q0 : __fmaf_rn(r, y, q0);
+            };
+            uint32_t packed[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+                    make_float2(quot(f[4 * q]), quot(f[4 * q + 1])), __NV_SATFINITE, __NV_E4M3);
+                const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+                    make_float2(quot(f[4 * q + 2]), quot(f[4 * q + 3])), __NV_SATFINITE,
+                    __NV_E4M3);
+                packed[q] = (uint32_t)lo | ((uint32_t)hi << 16);
+            }
+            const bool block_lead = (lane % GL) == 0;
+            const int64_t b = e / a.block;
+            for (int k = 0; k < K; ++k) {
+                const int32_t d = __shfl_sync(0xffffffffu, my_row, k);
+                if (d < 0 || !active) continue;
+                uint8_t *dst = a.q + (int64_t)d * a.H + e;
+                asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(dst), "r"(packed[0]),
+                             "r"(packed[1])
+                             : "memory");
+                if (block_lead) a.scales[(int64_t)d * nb + b] = scale;
+            }
+        }
+    }
+}
+
 int pick_chunk(int64_t row_bytes, int *n_chunks)
 {
     // split the row into m equal chunks of at most kMaxChunk bytes when the
@@ -314,6 +443,59 @@ MOE_EXPORT int moe_dispatch_dedup(const void *x, int64_t S, int64_t H, int dtype
     a.src_rows = max_rows;
     a.dst_rows = S * (int64_t)K;
     return launch_copy(a, (cudaStream_t)stream);
+}
+
+MOE_EXPORT int moe_dispatch_quant_fp8(const void *x, int64_t S, int64_t H, int K,
+                                      const int64_t *tok_map, int block, void *packed_q,
+                                      float *packed_scales, moe_stream_t stream)
+{
+    if (S < 0 || H < 1 || K < 1 || K > 32) return MOE_EINVAL;
+    if (block != 16 && block != 32 && block != 64 && block != 128 && block != 256)
+        return MOE_EINVAL;
+    if (H % block) return MOE_EINVAL;
+    if (S == 0) return MOE_OK;
+    if (!x || !tok_map || !packed_q || !packed_scales) return MOE_EINVAL;
+    if (!aligned16(x) || !aligned16(packed_q) || (reinterpret_cast<uintptr_t>(packed_scales) & 3u))
+        return MOE_EALIGN;
+    QuantArgs a = {};
+    a.x = static_cast<const uint8_t *>(x);
+    a.S = S;
+    a.H = H;
+    a.K = K;
+    a.tok_map = tok_map;
+    a.dst_rows = S * (int64_t)K;
+    a.block = block;
+    a.iters = (int)((H + 255) / 256);
+    a.slices = (a.iters + kQMaxIters - 1) / kQMaxIters;
+    a.R = (a.iters + a.slices - 1) / a.slices;
+    a.q = static_cast<uint8_t *>(packed_q);
+    a.scales = packed_scales;
+    void (*fn)(QuantArgs) = nullptr;
+    static KernelCache caches[5];
+    KernelCache *cache = nullptr;
+    switch (block) {
+    case 16: fn = dispatch_quant_kernel<2>; cache = &caches[0]; break;
+    case 32: fn = dispatch_quant_kernel<4>; cache = &caches[1]; break;
+    case 64: fn = dispatch_quant_kernel<8>; cache = &caches[2]; break;
+    case 128: fn = dispatch_quant_kernel<16>; cache = &caches[3]; break;
+    default: fn = dispatch_quant_kernel<32>; cache = &caches[4]; break;
+    }
+    int per_sm = 0;
+    cudaError_t err = prepare_kernel(fn, 0, kQThreads, *cache, &per_sm);
+    if (err != cudaSuccess || per_sm < 1) {
+        set_cuda_error(err != cudaSuccess ? err : cudaErrorInvalidConfiguration);
+        return MOE_ECUDA;
+    }
+    const int64_t units = S * a.slices;
+    int64_t blocks = (units + kQThreads / 32 - 1) / (kQThreads / 32);
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    if (blocks > cap) blocks = cap;
+    err = launch_pdl(fn, dim3((unsigned)blocks), dim3(kQThreads), 0, (cudaStream_t)stream, a);
+    if (err != cudaSuccess) {
+        set_cuda_error(err);
+        return MOE_ECUDA;
+    }
+    return check_launch();
 }
 
 namespace moe {

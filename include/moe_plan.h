@@ -198,6 +198,26 @@ int moe_dispatch(const void *x, int64_t S, int64_t H, int dtype, int K,
                  int64_t n_scales, float *packed_scales, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Quantising dispatch  [mori #448: Fp8BlockwiseQuant notes (per-block amax,
+ * f32 scale, fp8 cast; block amax by a lane butterfly) and scale_dim note].
+ * Reads each bf16 row once and writes it, quantised, to its K packed rows:
+ *   for every block b of `block` elements of x[s]:
+ *     scale = amax_b / 448 (1 if the block is all zero), IEEE f32 division
+ *     packed_q[r, j]            = E4M3(x[s, j] / scale)  (nearest even,
+ *                                 saturating to +-448; IEEE f32 division)
+ *     packed_scales[r, b]       = scale
+ *   for every r = tok_map[s,k] >= 0.  x must hold finite values.
+ * x              bf16 [S, H]; H a multiple of block
+ * block          16, 32, 64, 128 or 256
+ * packed_q       uint8 [>= off[E], H] (E4M3 codes); S*K rows always suffice
+ * packed_scales  f32 [>= off[E], H / block]
+ * Alignment: x and packed_q 16-byte aligned, packed_scales 4-byte aligned.
+ * ---------------------------------------------------------------------- */
+int moe_dispatch_quant_fp8(const void *x, int64_t S, int64_t H, int K,
+                           const int64_t *tok_map, int block, void *packed_q,
+                           float *packed_scales, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Dedup dispatch  [mori #448: ballot-dedup send, then convert_dispatch_output
  * per (received token, k)].  Two stages on `stream`:
  *   grp_x[r, :]                = x[grp_src[r] / K, :]          r < R = goff[G]

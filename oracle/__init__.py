@@ -74,6 +74,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_expert_scale_bf16.restype = None
     lib.oracle_expert_dequant_fp8.argtypes = [P, P, I64, I64, I32, P]
     lib.oracle_expert_dequant_fp8.restype = None
+    lib.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+    lib.oracle_f32_to_e4m3.restype = ctypes.c_uint8
+    lib.oracle_quant_fp8.argtypes = [P, I64, I64, I32, P, P]
+    lib.oracle_quant_fp8.restype = None
     return lib
 
 
@@ -204,6 +208,23 @@ def expert_scale_bf16(packed: np.ndarray, off: np.ndarray, c: np.ndarray, lib=No
     y = np.zeros_like(packed)
     lib.oracle_expert_scale_bf16(_p(packed), _p(off), len(c), _p(c), H, _p(y))
     return y
+
+
+def quant_fp8(x_bf16: np.ndarray, block: int, lib=None):
+    """Blockwise E4M3 codes and f32 scales of bf16 rows: (q uint8 [S,H],
+    scales f32 [S, H/block])."""
+    lib = lib or load()
+    x = _c(x_bf16, np.uint16)
+    S, H = x.shape
+    q = np.zeros((S, H), np.uint8)
+    sc = np.zeros((S, H // block), np.float32)
+    if S:
+        lib.oracle_quant_fp8(_p(x), S, H, block, _p(q), _p(sc))
+    return q, sc
+
+
+def f32_to_e4m3(v: float, lib=None) -> int:
+    return int((lib or load()).oracle_f32_to_e4m3(float(v)))
 
 
 def expert_dequant_fp8(q: np.ndarray, scales: np.ndarray, block: int, lib=None):

@@ -102,6 +102,42 @@ ORACLE_API float oracle_e4m3_to_f32(uint8_t q)
     return (float)(sign ? -v : v);
 }
 
+/* Round a binary32 value to E4M3, to nearest with ties to even, saturating to
+ * +-448 (the largest finite code); NaN maps to the NaN code.  Written from the
+ * format definition: the representable magnitudes are m/8 * 2^-6 (m = 0..7,
+ * subnormal) and (1 + m/8) * 2^(e-7) (e = 1..15, excluding e=15,m=7).  The
+ * candidate codes are walked in increasing magnitude and the nearest is
+ * taken; the exact midpoint goes to the code with an even mantissa. */
+ORACLE_API uint8_t oracle_f32_to_e4m3(float f)
+{
+    if (f != f)
+        return 0x7f;
+    uint8_t sign = signbit(f) ? 0x80 : 0x00;
+    double a = fabs((double)f);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7e);
+    /* largest code whose magnitude is <= a, then compare with the next */
+    uint8_t lo = 0;
+    for (uint8_t c = 1; c <= 0x7e; ++c) {
+        if ((double)oracle_e4m3_to_f32(c) <= a)
+            lo = c;
+        else
+            break;
+    }
+    if (lo == 0x7e)
+        return (uint8_t)(sign | lo);
+    double vlo = oracle_e4m3_to_f32(lo);
+    double vhi = oracle_e4m3_to_f32((uint8_t)(lo + 1));
+    uint8_t code;
+    if (a - vlo < vhi - a)
+        code = lo;
+    else if (a - vlo > vhi - a)
+        code = (uint8_t)(lo + 1);
+    else
+        code = (lo & 1) ? (uint8_t)(lo + 1) : lo;  /* tie: even mantissa */
+    return (uint8_t)(sign | code);
+}
+
 static float load_elem(const void *base, int dt, int64_t i)
 {
     if (dt == ODT_BF16)
@@ -265,6 +301,34 @@ ORACLE_API void oracle_dispatch(const uint8_t *rows, int64_t S, int64_t row_byte
             int64_t row = tok_map[s * K + k];
             if (row >= 0)
                 memcpy(packed + row * row_bytes, rows + s * row_bytes, (size_t)row_bytes);
+        }
+}
+
+/* ------------------------------------------------------------------------
+ * Blockwise fp8 quantisation of bf16 rows [mori448 Fp8BlockwiseQuant note;
+ * the note's formula is garbled, the reading taken: per block of `block`
+ * elements, scale = amax / 448 (1 when the block is all zero) and
+ * code = E4M3(v / scale), both divisions in f32].  The quantising dispatch
+ * is this function followed by oracle_dispatch of the codes and the scales.
+ * ---------------------------------------------------------------------- */
+ORACLE_API void oracle_quant_fp8(const uint16_t *x, int64_t S, int64_t H, int block,
+                                 uint8_t *q, float *scales)
+{
+    int64_t nb = H / block;
+    for (int64_t s = 0; s < S; ++s)
+        for (int64_t b = 0; b < nb; ++b) {
+            float amax = 0.0f;
+            for (int j = 0; j < block; ++j) {
+                float v = fabsf(oracle_bf16_to_f32(x[s * H + b * block + j]));
+                if (v > amax)
+                    amax = v;
+            }
+            float scale = (amax > 0.0f) ? amax / 448.0f : 1.0f;
+            scales[s * nb + b] = scale;
+            for (int j = 0; j < block; ++j) {
+                float v = oracle_bf16_to_f32(x[s * H + b * block + j]);
+                q[s * H + b * block + j] = oracle_f32_to_e4m3(v / scale);
+            }
         }
 }
 

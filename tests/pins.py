@@ -420,6 +420,68 @@ def pin_expert_stages(lib):
     assert np.array_equal(y8, ref)
 
 
+def _e4m3_torch(vals: np.ndarray) -> np.ndarray:
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(vals, np.float32)).to(
+        torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def pin_e4m3_encode(lib):
+    """The oracle's E4M3 encoder against torch's CPU float8_e4m3fn cast
+    (round to nearest, ties to even) wherever torch does not overflow
+    (|v| < 464): every bf16 value, every midpoint between neighbouring codes
+    and its f32 neighbours, and random f32 values; plus saturation and NaN,
+    where the oracle follows the satfinite rule."""
+    import workloads
+    hi = np.arange(1 << 16, dtype=np.uint32)
+    bf = (hi << 16).view(np.float32)
+    bf = bf[np.isfinite(bf) & (np.abs(bf) < 464)]
+    codes = np.arange(0x7f, dtype=np.uint8)
+    import torch
+    mags = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    mids = ((mags[:-1] + mags[1:]) / 2).astype(np.float32)
+    near = np.concatenate([mids, np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(1e9))])
+    near = np.concatenate([near, -near])
+    rnd = (np.exp(workloads.uniform01(7, 60, 20000) * 18 - 12) *
+           np.where(workloads.uniform01(7, 61, 20000) < 0.5, -1, 1)).astype(np.float32)
+    rnd = rnd[np.abs(rnd) < 464]
+    vals = np.concatenate([bf, near, rnd]).astype(np.float32)
+    got = np.array([oracle.f32_to_e4m3(float(v), lib=lib) for v in vals], np.uint8)
+    assert np.array_equal(got, _e4m3_torch(vals))
+    assert oracle.f32_to_e4m3(450.0, lib=lib) == 0x7E
+    assert oracle.f32_to_e4m3(1e30, lib=lib) == 0x7E
+    assert oracle.f32_to_e4m3(-1e30, lib=lib) == 0xFE
+    assert oracle.f32_to_e4m3(float("nan"), lib=lib) & 0x7F == 0x7F
+
+
+def pin_quant_fp8_rule(lib):
+    """Blockwise quantisation: equals the same rule applied with numpy f32
+    division and torch's cast (a library cross-check); the largest element of
+    every block maps to +-448; an all-zero block has scale 1 and zero codes;
+    dequantised values are within E4M3's rounding error of the input."""
+    import workloads
+    S, H, block = 24, 512, 128
+    xf = workloads.activations_f32(9, S, H)
+    xf[3, :128] = 0.0                              # an all-zero block
+    xf[5, 128:256] *= 1e-6                         # a tiny block (subnormal codes)
+    x = workloads.to_bf16_bits(xf)
+    q, sc = oracle.quant_fp8(x, block, lib=lib)
+    xv = bf16_bits_to_f64(x).astype(np.float32).reshape(S, H // block, block)
+    amax = np.abs(xv).max(axis=2)
+    ref_sc = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    assert np.array_equal(sc, ref_sc)
+    ref_q = _e4m3_torch((xv / ref_sc[:, :, None]).astype(np.float32).reshape(S, H))
+    assert np.array_equal(q, ref_q)
+    assert np.all(sc[3, 0] == 1.0) and np.all(q[3, :128] == 0)
+    import torch
+    deq = torch.from_numpy(q).view(torch.float8_e4m3fn).float().numpy().reshape(S, H // block, block)
+    top = np.abs(deq).max(axis=2)
+    assert np.all((top == 448.0) | (amax == 0))
+    back = deq * sc[:, :, None]
+    err = np.abs(back - xv)
+    assert np.all(err <= np.abs(xv) * 2.0 ** -4 + sc[:, :, None] * 2.0 ** -10 * 1.0001)
+
+
 ALL_PINS = [
     pin_plan_bruteforce, pin_plan_hand_example, pin_plan_invariants,
     pin_group_plan_bruteforce, pin_group_plan_invariants,
@@ -427,5 +489,5 @@ ALL_PINS = [
     pin_combine_exact_rational, pin_combine_identity_telescopes,
     pin_combine_expert_scale_closed_form, pin_combine_single_k_is_copy, pin_combine_k_order,
     pin_combine_dedup_closed_forms,
-    pin_bf16_rounding, pin_e4m3_table, pin_expert_stages,
+    pin_bf16_rounding, pin_e4m3_table, pin_expert_stages, pin_e4m3_encode, pin_quant_fp8_rule,
 ]

@@ -115,3 +115,18 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
 def test_device_errors_rejects_null(L):
     assert L.moe_device_errors(None) == EINVAL
     _ = ctypes  # noqa
+
+
+def test_quant_dispatch_validation(L):
+    q = lambda **k: L.moe_dispatch_quant_fp8(k.get("x", FAKE), k.get("S", 4), k.get("H", 256),
+                                             k.get("K", 2), k.get("tm", FAKE), k.get("block", 128),
+                                             k.get("q", FAKE), k.get("sc", FAKE), None)
+    assert q(S=0) == OK
+    assert q(block=100) == EINVAL
+    assert q(block=512) == EINVAL
+    assert q(H=192) == EINVAL                 # not a multiple of the block
+    assert q(K=0) == EINVAL
+    assert q(tm=None) == EINVAL
+    assert q(x=MIS) == EALIGN
+    assert q(q=MIS) == EALIGN
+    assert q(sc=FAKE + 2) == EALIGN

@@ -72,6 +72,14 @@ MUTANTS = [
      [pins.pin_expert_stages, pins.pin_combine_expert_scale_closed_form]),
     ("dequant_wrong_block", "scales[r * nb + j / block]", "scales[r * nb + j % nb]",
      [pins.pin_expert_stages]),
+    ("e4m3_encode_ties_up", "code = (lo & 1) ? (uint8_t)(lo + 1) : lo;  /* tie: even mantissa */",
+     "code = (uint8_t)(lo + 1);", [pins.pin_e4m3_encode]),
+    ("e4m3_encode_overflow_to_nan", "if (a >= 448.0)\n        return (uint8_t)(sign | 0x7e);",
+     "if (a >= 448.0)\n        return (uint8_t)(sign | 0x7f);", [pins.pin_e4m3_encode]),
+    ("quant_scale_off_by_max", "float scale = (amax > 0.0f) ? amax / 448.0f : 1.0f;",
+     "float scale = (amax > 0.0f) ? amax / 240.0f : 1.0f;", [pins.pin_quant_fp8_rule]),
+    ("quant_multiplies", "q[s * H + b * block + j] = oracle_f32_to_e4m3(v / scale);",
+     "q[s * H + b * block + j] = oracle_f32_to_e4m3(v * (1.0f / scale));", [pins.pin_quant_fp8_rule]),
 ]
 
 

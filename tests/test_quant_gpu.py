@@ -1,0 +1,127 @@
+"""Quantising dispatch (bf16 rows -> blockwise E4M3 codes + f32 scales in the
+packed rows) against the CPU oracle: codes, scales and untouched rows are
+compared bit-exactly.  The divisions and the cast are IEEE f32 and
+round-to-nearest-even on both sides, so no tolerance is needed."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+from tests import gpu_path  # noqa: E402
+
+
+def _run(x_bits: np.ndarray, idx: np.ndarray, E: int, block: int):
+    import combine_moe_plan_02_gb300 as moe
+    S, H = x_bits.shape
+    K = idx.shape[1]
+    dev = torch.device("cuda")
+    x = torch.from_numpy(x_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    plan = moe.moe_plan(torch.from_numpy(np.ascontiguousarray(idx)).to(dev), E)
+    q = gpu_path.poisoned((max(S * K, 1), H), torch.uint8)
+    sc = gpu_path.poisoned((max(S * K, 1), H // block), torch.float32)
+    moe.moe_dispatch_quant_fp8(x, plan.tok_map, block=block, packed_q=q, packed_scales=sc)
+    torch.cuda.synchronize()
+    assert moe.moe_device_errors() == 0
+    return q.cpu().numpy(), sc.cpu().numpy(), int(plan.off[-1].item())
+
+
+def _check(x_bits, idx, E, block):
+    q, sc, V = _run(x_bits, idx, E, block)
+    p = oracle.plan(idx, E)
+    q0, sc0 = oracle.quant_fp8(x_bits, block)
+    ref_q = oracle.dispatch(q0, p["tok_map"], V)
+    ref_sc = oracle.dispatch(sc0, p["tok_map"], V)
+    assert V == int(p["off"][-1])
+    assert np.array_equal(q[:V], ref_q)
+    assert np.array_equal(sc[:V].view(np.uint32), ref_sc.view(np.uint32))
+    assert np.all(q[V:] == gpu_path.POISON)          # rows past off[E] untouched
+
+
+@pytest.mark.timeout(600)
+def test_moonep_shape():
+    wl = workloads.make("moonep", seed=21, S=600)
+    _check(wl.x, wl.topk_idx, wl.E, 128)
+
+
+@pytest.mark.timeout(600)
+@pytest.mark.parametrize("S", workloads.FP8_SWEEP_TOKENS)
+def test_small_token_shape(S):
+    """H=6144, E=256, K=8 (the fp8 latency workload), bf16 input rows."""
+    wl = workloads.make("moonep", seed=S, S=S, H=6144, E=256, K=8)
+    _check(wl.x, wl.topk_idx, wl.E, 128)
+
+
+@pytest.mark.timeout(600)
+@pytest.mark.parametrize("block", [16, 32, 64, 128, 256])
+def test_block_sizes(block):
+    wl = workloads.make("moonep", seed=block, S=257, H=768, E=16, K=3)
+    _check(wl.x, wl.topk_idx, wl.E, block)
+
+
+@pytest.mark.timeout(600)
+def test_edge_rows():
+    """All-zero blocks (scale 1), tiny blocks (subnormal codes), huge values,
+    a ragged H (not a multiple of 256), unused entries."""
+    wl = workloads.make("moonep", seed=3, S=90, H=384, E=8, K=4)
+    xf = workloads.activations_f32(3, 90, 384)
+    xf[0] = 0.0
+    xf[1, :128] *= 1e-30
+    xf[2, 128:256] *= 1e30
+    xf[4, ::7] = 448.0
+    x = workloads.to_bf16_bits(xf)
+    idx = wl.topk_idx.copy()
+    idx[::5, 2] = -1
+    _check(x, idx, wl.E, 128)
+
+
+@pytest.mark.timeout(600)
+def test_every_bf16_value_encodes_like_the_oracle():
+    """Each 128-block holds 448 (so scale = 1 and the codes are the plain
+    E4M3 encoding of the inputs) and 127 bf16 values; together the rows cover
+    every finite bf16 value of magnitude <= 448."""
+    allbits = np.arange(1 << 16, dtype=np.uint32)
+    vals = (allbits << 16).view(np.float32)
+    keep = np.isfinite(vals) & (np.abs(vals) <= 448)
+    bits = allbits[keep].astype(np.uint16)
+    per = 127
+    nrows_blocks = -(-bits.size // per)
+    pad = nrows_blocks * per - bits.size
+    bits = np.concatenate([bits, np.zeros(pad, np.uint16)]).reshape(nrows_blocks, per)
+    lead = np.full((nrows_blocks, 1), 0x43E0, np.uint16)     # bf16 448.0
+    blocks = np.concatenate([lead, bits], axis=1)             # [nb, 128]
+    H = 1024
+    nb_row = H // 128
+    nrows = -(-blocks.shape[0] // nb_row)
+    extra = nrows * nb_row - blocks.shape[0]
+    filler = np.tile(np.concatenate([[0x43E0], np.zeros(127, np.uint16)]).astype(np.uint16),
+                     (extra, 1))
+    x = np.concatenate([blocks, filler]).reshape(nrows, H)
+    idx = np.zeros((nrows, 1), np.int32)
+    q, sc, V = _run(x, idx, 1, 128)
+    assert np.all(sc[:V] == 1.0)
+    ref = np.array([oracle.f32_to_e4m3(float(v)) for v in
+                    (x.astype(np.uint32) << 16).view(np.float32).reshape(-1)], np.uint8)
+    assert np.array_equal(q[:V].reshape(-1), ref)
+
+
+@pytest.mark.timeout(600)
+def test_quantised_dispatch_matches_dispatch_of_quantised_rows():
+    """The fused path equals quantising with the oracle and dispatching the
+    codes and scales with the byte-copy dispatch (which forwards scales)."""
+    import combine_moe_plan_02_gb300 as moe
+    wl = workloads.make("moonep", seed=5, S=128, H=6144, E=256, K=8)
+    q0, sc0 = oracle.quant_fp8(wl.x, 128)
+    dev = torch.device("cuda")
+    plan = moe.moe_plan(torch.from_numpy(wl.topk_idx).to(dev), wl.E)
+    pq, ps = moe.moe_dispatch(torch.from_numpy(q0).to(dev).view(torch.float8_e4m3fn),
+                              plan.tok_map, x_scales=torch.from_numpy(sc0).to(dev))
+    x = torch.from_numpy(wl.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    fq, fs = moe.moe_dispatch_quant_fp8(x, plan.tok_map)
+    torch.cuda.synchronize()
+    assert torch.equal(pq.view(torch.uint8), fq.view(torch.uint8))
+    assert torch.equal(ps.view(torch.int32), fs.view(torch.int32))
