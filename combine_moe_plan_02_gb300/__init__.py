@@ -23,7 +23,8 @@ __all__ = [
     "moe_plan", "moe_group_plan", "moe_dispatch", "moe_dispatch_dedup", "moe_dispatch_quant_fp8",
     "moe_combine",
     "moe_combine_dedup", "moe_plan_workspace_size", "moe_group_plan_workspace_size",
-    "moe_device_errors", "Plan", "GroupPlan", "MoeError", "lib",
+    "moe_device_errors", "moe_plan_capacity", "Plan", "GroupPlan", "CapacityPlan", "MoeError",
+    "lib",
 ]
 
 
@@ -123,6 +124,42 @@ def moe_plan(topk_idx: torch.Tensor, E: int, *, out: Optional[Plan] = None,
     return out
 
 
+class CapacityPlan(NamedTuple):
+    cnt: torch.Tensor          # int32 [E] rows filled per bucket
+    off: torch.Tensor          # int64 [E+1] = e * capacity
+    packed_src: torch.Tensor   # int32 [E*capacity]
+    tok_map: torch.Tensor      # int64 [S, K], -1 for dropped entries
+    n_invalid: torch.Tensor    # int32 [1]
+    n_dropped: torch.Tensor    # int32 [1]
+    capacity: int
+
+
+def moe_plan_capacity(topk_idx: torch.Tensor, E: int, capacity: int, *,
+                      out: Optional[CapacityPlan] = None,
+                      workspace: Optional[torch.Tensor] = None, stream=None) -> CapacityPlan:
+    """Plan into padded buckets of `capacity` rows; entries past a bucket's
+    capacity (later tokens first to go) are dropped to -1."""
+    if topk_idx.dtype != torch.int32 or topk_idx.dim() != 2:
+        raise TypeError("topk_idx must be int32 [S, K]")
+    S, K = topk_idx.shape
+    dev = topk_idx.device
+    if out is None:
+        out = CapacityPlan(torch.empty(E, dtype=torch.int32, device=dev),
+                           torch.empty(E + 1, dtype=torch.int64, device=dev),
+                           torch.empty(E * capacity, dtype=torch.int32, device=dev),
+                           torch.empty(S, K, dtype=torch.int64, device=dev),
+                           torch.empty(1, dtype=torch.int32, device=dev),
+                           torch.empty(1, dtype=torch.int32, device=dev), capacity)
+    L = lib()
+    nws = int(L.moe_plan_workspace_size(S, K, E))
+    ws = _workspace(nws, dev, workspace)
+    _abi.check("moe_plan_capacity", L.moe_plan_capacity(
+        _ptr(topk_idx), S, K, E, capacity, _ptr(out.cnt), _ptr(out.off), _ptr(out.packed_src),
+        _ptr(out.tok_map), _ptr(out.n_invalid), _ptr(out.n_dropped), _ptr(ws), nws,
+        _stream(stream)))
+    return out
+
+
 def moe_group_plan(topk_idx: torch.Tensor, tok_map: torch.Tensor, E: int, group_size: int, *,
                    out: Optional[GroupPlan] = None, workspace: Optional[torch.Tensor] = None,
                    stream=None) -> GroupPlan:
@@ -162,9 +199,11 @@ def moe_dispatch(x: torch.Tensor, tok_map: torch.Tensor, *, packed_x: Optional[t
         n_scales = x_scales.shape[1]
         if packed_scales is None:
             packed_scales = torch.empty(S * K, n_scales, dtype=torch.float32, device=x.device)
+    if packed_scales is not None and packed_scales.shape[0] < packed_x.shape[0]:
+        raise ValueError("packed_scales needs as many rows as packed_x")
     _abi.check("moe_dispatch", lib().moe_dispatch(
-        _ptr(x), S, H, _dt(x), K, _ptr(tok_map), _ptr(packed_x), _ptr(x_scales), n_scales,
-        _ptr(packed_scales), _stream(stream)))
+        _ptr(x), S, H, _dt(x), K, _ptr(tok_map), _ptr(packed_x), packed_x.shape[0],
+        _ptr(x_scales), n_scales, _ptr(packed_scales), _stream(stream)))
     return packed_x, packed_scales
 
 
@@ -181,8 +220,9 @@ def moe_dispatch_quant_fp8(x: torch.Tensor, tok_map: torch.Tensor, *, block: int
         packed_q = torch.empty(S * K, H, dtype=torch.float8_e4m3fn, device=x.device)
     if packed_scales is None:
         packed_scales = torch.empty(S * K, H // block, dtype=torch.float32, device=x.device)
+    rows = min(packed_q.shape[0], packed_scales.shape[0])
     _abi.check("moe_dispatch_quant_fp8", lib().moe_dispatch_quant_fp8(
-        _ptr(x), S, H, K, _ptr(tok_map), block, _ptr(packed_q), _ptr(packed_scales),
+        _ptr(x), S, H, K, _ptr(tok_map), block, _ptr(packed_q), _ptr(packed_scales), rows,
         _stream(stream)))
     return packed_q, packed_scales
 
@@ -212,7 +252,7 @@ def moe_combine(y: torch.Tensor, topk_w: torch.Tensor, tok_map: torch.Tensor, *,
     if out is None:
         out = torch.empty(S, H, dtype=out_dtype, device=y.device)
     _abi.check("moe_combine", lib().moe_combine(
-        _ptr(y), _dt(y), _ptr(topk_w), _ptr(tok_map), S, H, K, _ptr(out), _dt(out),
+        _ptr(y), y.shape[0], _dt(y), _ptr(topk_w), _ptr(tok_map), S, H, K, _ptr(out), _dt(out),
         _stream(stream)))
     return out
 

@@ -244,21 +244,22 @@ bool combine_dtype_ok(int dt) { return dt == MOE_BF16 || dt == MOE_F32; }
 
 using namespace moe;
 
-MOE_EXPORT int moe_combine(const void *y, int in_dtype, const float *topk_w,
+MOE_EXPORT int moe_combine(const void *y, int64_t y_rows, int in_dtype, const float *topk_w,
                            const int64_t *tok_map, int64_t S, int64_t H, int K, void *out,
                            int out_dtype, moe_stream_t stream)
 {
     if (!combine_dtype_ok(in_dtype) || !combine_dtype_ok(out_dtype)) return MOE_EINVAL;
     if (S < 0 || H < 1 || K < 1 || K > 32) return MOE_EINVAL;
     if (S == 0) return MOE_OK;
-    if (!y || !topk_w || !tok_map || !out) return MOE_EINVAL;
+    if (!y || !topk_w || !tok_map || !out || y_rows < 1 || y_rows >= ((int64_t)1 << 31))
+        return MOE_EINVAL;
     if (H % 8 || !aligned16(y) || !aligned16(out)) return MOE_EALIGN;
     CombineArgs a = {};
     a.y = static_cast<const uint8_t *>(y);
     a.w = topk_w;
     a.map = tok_map;
     a.rows = S;
-    a.y_rows = S * (int64_t)K;
+    a.y_rows = y_rows;
     a.K = K;
     a.H = H;
     a.steps = H / 8;

@@ -376,13 +376,14 @@ int launch_copy(CopyArgs &a, cudaStream_t stream)
 using namespace moe;
 
 MOE_EXPORT int moe_dispatch(const void *x, int64_t S, int64_t H, int dtype, int K,
-                            const int64_t *tok_map, void *packed_x, const float *x_scales,
-                            int64_t n_scales, float *packed_scales, moe_stream_t stream)
+                            const int64_t *tok_map, void *packed_x, int64_t packed_rows,
+                            const float *x_scales, int64_t n_scales, float *packed_scales,
+                            moe_stream_t stream)
 {
     const int es = elem_size(dtype);
     if (es == 0 || S < 0 || H < 1 || K < 1 || K > 32 || n_scales < 0) return MOE_EINVAL;
     if (S == 0) return MOE_OK;
-    if (!x || !tok_map || !packed_x) return MOE_EINVAL;
+    if (!x || !tok_map || !packed_x || packed_rows < 1) return MOE_EINVAL;
     if (n_scales > 0 && (!x_scales || !packed_scales)) return MOE_EINVAL;
     const int64_t row_bytes = H * es;
     if (row_bytes % 16 || !aligned16(x) || !aligned16(packed_x)) return MOE_EALIGN;
@@ -399,7 +400,7 @@ MOE_EXPORT int moe_dispatch(const void *x, int64_t S, int64_t H, int dtype, int 
     a.src_div = 1;
     a.rows = S;
     a.src_rows = S;
-    a.dst_rows = S * (int64_t)K;
+    a.dst_rows = packed_rows;
     a.ssrc = reinterpret_cast<const uint8_t *>(x_scales);
     a.sdst = reinterpret_cast<uint8_t *>(packed_scales);
     a.scale_bytes = (int)(n_scales * 4);
@@ -447,14 +448,15 @@ MOE_EXPORT int moe_dispatch_dedup(const void *x, int64_t S, int64_t H, int dtype
 
 MOE_EXPORT int moe_dispatch_quant_fp8(const void *x, int64_t S, int64_t H, int K,
                                       const int64_t *tok_map, int block, void *packed_q,
-                                      float *packed_scales, moe_stream_t stream)
+                                      float *packed_scales, int64_t packed_rows,
+                                      moe_stream_t stream)
 {
     if (S < 0 || H < 1 || K < 1 || K > 32) return MOE_EINVAL;
     if (block != 16 && block != 32 && block != 64 && block != 128 && block != 256)
         return MOE_EINVAL;
     if (H % block) return MOE_EINVAL;
     if (S == 0) return MOE_OK;
-    if (!x || !tok_map || !packed_q || !packed_scales) return MOE_EINVAL;
+    if (!x || !tok_map || !packed_q || !packed_scales || packed_rows < 1) return MOE_EINVAL;
     if (!aligned16(x) || !aligned16(packed_q) || (reinterpret_cast<uintptr_t>(packed_scales) & 3u))
         return MOE_EALIGN;
     QuantArgs a = {};
@@ -463,7 +465,7 @@ MOE_EXPORT int moe_dispatch_quant_fp8(const void *x, int64_t S, int64_t H, int K
     a.H = H;
     a.K = K;
     a.tok_map = tok_map;
-    a.dst_rows = S * (int64_t)K;
+    a.dst_rows = packed_rows;
     a.block = block;
     a.iters = (int)((H + 255) / 256);
     a.slices = (a.iters + kQMaxIters - 1) / kQMaxIters;

@@ -105,6 +105,8 @@ struct RankOut {
     int32_t *n_invalid;    // [1] (direct plan) or null
     const int64_t *tok_map;  // group plan: tok_map of the direct plan
     int64_t *grp_tok_map;    // group plan: [rows, K]
+    int64_t cap;             // > 0: padded buckets of cap rows, later entries dropped
+    int32_t *n_dropped;      // [1] with cap > 0
 };
 
 // Key of the 32 entries [c, c+32) of a chunk, one per lane: the slot key, -1
@@ -411,21 +413,31 @@ __global__ void __launch_bounds__(kThreads, 1) plan_rank_kernel(Key key, int nke
     }
     __syncthreads();
 
-    // (c) exclusive scan over keys (nkeys <= kThreads: one key per thread)
+    // (c) exclusive scan over keys (nkeys <= kThreads: one key per thread).
+    // s_base holds the first rank of this tile in each key; with a capacity
+    // the bucket of key e starts at e * cap instead of at the scan.
     const int e = threadIdx.x;
     const int64_t tot = (e < nkeys) ? s_tot[e] : 0;
     int64_t total;
     const int64_t offe = block_exclusive_scan(tot, s_scan, total);
     if (e < nkeys) {
-        s_base[e] = offe + s_bef[e];
+        s_base[e] = (o.cap > 0 ? 0 : offe) + s_bef[e];
         if (t == 0) {
-            o.cnt[e] = (int32_t)tot;
-            o.off[e] = offe;
+            o.cnt[e] = (int32_t)(o.cap > 0 ? min(tot, o.cap) : tot);
+            o.off[e] = o.cap > 0 ? (int64_t)e * o.cap : offe;
         }
     }
     if (t == 0 && threadIdx.x == 0) {
-        o.off[nkeys] = total;
+        o.off[nkeys] = o.cap > 0 ? (int64_t)nkeys * o.cap : total;
         if (o.n_invalid) *o.n_invalid = s_inval;
+    }
+    if (o.cap > 0 && t == 0) {
+        // entries that do not fit: sum over keys of max(0, count - cap)
+        __syncthreads();  // every thread has read the first scan's s_scan
+        int64_t dropped_total;
+        (void)block_exclusive_scan(e < nkeys ? max((int64_t)0, tot - o.cap) : 0, s_scan,
+                                   dropped_total);
+        if (threadIdx.x == 0) *o.n_dropped = (int32_t)dropped_total;
     }
 
     // (d) exclusive scan over the 32 warps, per key, relative to the tile
@@ -447,7 +459,10 @@ __global__ void __launch_bounds__(kThreads, 1) plan_rank_kernel(Key key, int nke
         const int k = (c == wbegin) ? k_first : key.chunk_key(i, i < wend);
         const unsigned peers = __match_any_sync(0xffffffffu, k);
         int64_t row = -1;
-        if (k >= 0) row = s_base[k] + my_wc[k] + __popc(peers & lanemask_lt());
+        if (k >= 0) {
+            row = s_base[k] + my_wc[k] + __popc(peers & lanemask_lt());
+            if (o.cap > 0) row = row < o.cap ? (int64_t)k * o.cap + row : -1;
+        }
         __syncwarp();
         if (k >= 0 && lane == __ffs(peers) - 1) my_wc[k] += __popc(peers);
         __syncwarp();
@@ -516,7 +531,24 @@ MOE_EXPORT int moe_plan(const int32_t *topk_idx, int64_t S, int K, int E, int32_
     if (S > 0 && (!topk_idx || !packed_src || !tok_map)) return MOE_EINVAL;
     const PlanGeom g = plan_geom(S, K);
     const DirectKey key{topk_idx, E};
-    const RankOut o{cnt, off, tok_map, packed_src, n_invalid, nullptr, nullptr};
+    const RankOut o{cnt, off, tok_map, packed_src, n_invalid, nullptr, nullptr, 0, nullptr};
+    return run_plan(key, E, g, o, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+MOE_EXPORT int moe_plan_capacity(const int32_t *topk_idx, int64_t S, int K, int E,
+                                 int64_t capacity, int32_t *cnt, int64_t *off,
+                                 int32_t *packed_src, int64_t *tok_map, int32_t *n_invalid,
+                                 int32_t *n_dropped, void *workspace, size_t workspace_bytes,
+                                 moe_stream_t stream)
+{
+    if (int rc = check_plan_args(S, K, E)) return rc;
+    if (capacity < 1 || capacity * (int64_t)E >= ((int64_t)1 << 31)) return MOE_EINVAL;
+    if (!cnt || !off || !n_invalid || !n_dropped) return MOE_EINVAL;
+    if (S > 0 && (!topk_idx || !packed_src || !tok_map)) return MOE_EINVAL;
+    const PlanGeom g = plan_geom(S, K);
+    const DirectKey key{topk_idx, E};
+    const RankOut o{cnt, off, tok_map, packed_src, n_invalid, nullptr, nullptr, capacity,
+                    n_dropped};
     return run_plan(key, E, g, o, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
@@ -538,7 +570,7 @@ MOE_EXPORT int moe_group_plan(const int32_t *topk_idx, const int64_t *tok_map, i
         return MOE_EINVAL;
     const PlanGeom g = plan_geom(S, K);
     const GroupKey key{topk_idx, E, K, group_size};
-    const RankOut o{gcnt, goff, gtok_map, grp_src, nullptr, tok_map, grp_tok_map};
+    const RankOut o{gcnt, goff, gtok_map, grp_src, nullptr, tok_map, grp_tok_map, 0, nullptr};
     return run_plan(key, E / group_size, g, o, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
@@ -619,6 +651,6 @@ MOE_EXPORT int moe_plan_static_scratch(const int32_t *topk_idx, int64_t S, int K
     void *ws = nullptr;
     if (int rc = static_scratch_address(&ws)) return rc;
     const DirectKey key{topk_idx, E};
-    const RankOut o{cnt, off, tok_map, packed_src, n_invalid, nullptr, nullptr};
+    const RankOut o{cnt, off, tok_map, packed_src, n_invalid, nullptr, nullptr, 0, nullptr};
     return run_plan(key, E, g, o, ws, kStaticPlanScratchBytes, (cudaStream_t)stream);
 }

@@ -123,6 +123,26 @@ int moe_plan(const int32_t *topk_idx, int64_t S, int K, int E,
              moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Plan with a per-expert capacity  [mori #448 op-parity note: receive slots
+ * are capped; over-cap tokens take the drop path, with no out-of-bounds
+ * write].  Padded buckets: bucket e holds rows [e*capacity, (e+1)*capacity).
+ * Entry (s,k) keeps the slot it has in moe_plan's order if that slot is
+ * below capacity (earlier tokens first), else it is dropped:
+ *   cnt[e]        = min(entries of e, capacity);   off[e] = e * capacity
+ *   tok_map[s,k]  = e*capacity + slot, or -1 (dropped or id outside [0,E))
+ *   packed_src[e*capacity + slot] = s*K + k for kept entries; rows at or
+ *                   past cnt[e] in a bucket are left untouched
+ *   n_dropped[0]  = valid entries that did not fit
+ * packed_src int32 [E * capacity]; workspace as moe_plan_workspace_size.
+ * dispatch/combine then take packed_rows = E * capacity.
+ * Limits: as moe_plan; capacity >= 1 and E * capacity < 2^31.
+ * ---------------------------------------------------------------------- */
+int moe_plan_capacity(const int32_t *topk_idx, int64_t S, int K, int E, int64_t capacity,
+                      int32_t *cnt, int64_t *off, int32_t *packed_src, int64_t *tok_map,
+                      int32_t *n_invalid, int32_t *n_dropped, void *workspace,
+                      size_t workspace_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Plan without a caller-supplied workspace.  The pages have no counterpart:
  * this entry point exists for callers that cannot allocate device memory for
  * a workspace, such as a C or C++ host linking only this library with no
@@ -186,16 +206,20 @@ int moe_group_plan(const int32_t *topk_idx, const int64_t *tok_map, int64_t S, i
  * Rows of packed_x that no entry maps to are left untouched.
  *
  * x             [S, H] of `dtype` (a byte copy: any dtype of that size)
- * tok_map       int64 [S, K] from moe_plan; entries must be -1 or below S*K
- * packed_x      [>= off[E], H] of `dtype`; S*K rows always suffice
+ * tok_map       int64 [S, K] from moe_plan or moe_plan_capacity
+ * packed_x      [packed_rows, H] of `dtype`: off[E] rows suffice (S*K always
+ *               do for moe_plan; E*capacity for moe_plan_capacity); a map
+ *               entry at or past packed_rows is skipped and flagged (bit 1
+ *               of moe_device_errors)
  * x_scales      f32 [S, n_scales] or NULL when n_scales == 0
- * packed_scales f32 [>= off[E], n_scales] or NULL when n_scales == 0
+ * packed_scales f32 [packed_rows, n_scales] or NULL when n_scales == 0
  * Alignment: x, packed_x, x_scales, packed_scales 16-byte aligned; H*size
  * and n_scales*4 multiples of 16 (else MOE_EALIGN).
  * ---------------------------------------------------------------------- */
 int moe_dispatch(const void *x, int64_t S, int64_t H, int dtype, int K,
-                 const int64_t *tok_map, void *packed_x, const float *x_scales,
-                 int64_t n_scales, float *packed_scales, moe_stream_t stream);
+                 const int64_t *tok_map, void *packed_x, int64_t packed_rows,
+                 const float *x_scales, int64_t n_scales, float *packed_scales,
+                 moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Quantising dispatch  [mori #448: Fp8BlockwiseQuant notes (per-block amax,
@@ -209,13 +233,13 @@ int moe_dispatch(const void *x, int64_t S, int64_t H, int dtype, int K,
  *   for every r = tok_map[s,k] >= 0.  x must hold finite values.
  * x              bf16 [S, H]; H a multiple of block
  * block          16, 32, 64, 128 or 256
- * packed_q       uint8 [>= off[E], H] (E4M3 codes); S*K rows always suffice
- * packed_scales  f32 [>= off[E], H / block]
+ * packed_q       uint8 [packed_rows, H] (E4M3 codes); off[E] rows suffice
+ * packed_scales  f32 [packed_rows, H / block]
  * Alignment: x and packed_q 16-byte aligned, packed_scales 4-byte aligned.
  * ---------------------------------------------------------------------- */
 int moe_dispatch_quant_fp8(const void *x, int64_t S, int64_t H, int K,
                            const int64_t *tok_map, int block, void *packed_q,
-                           float *packed_scales, moe_stream_t stream);
+                           float *packed_scales, int64_t packed_rows, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Dedup dispatch  [mori #448: ballot-dedup send, then convert_dispatch_output
@@ -241,14 +265,15 @@ int moe_dispatch_dedup(const void *x, int64_t S, int64_t H, int dtype, int K, in
  * The sum is taken in f32 in increasing k, each product and each sum rounded
  * separately (no fused multiply-add); bf16 output rounds to nearest even.
  *
- * y       [>= off[E], H] of in_dtype (MOE_BF16 or MOE_F32)
+ * y       [y_rows, H] of in_dtype (MOE_BF16 or MOE_F32), 1 <= y_rows < 2^31;
+ *         a map entry at or past y_rows drops its term and is flagged (bit 2)
  * topk_w  f32 [S, K]; tok_map int64 [S, K] from moe_plan
  * out     [S, H] of out_dtype (MOE_BF16 or MOE_F32)
  * Alignment: y, out 16-byte aligned; H a multiple of 8.
  * ---------------------------------------------------------------------- */
-int moe_combine(const void *y, int in_dtype, const float *topk_w, const int64_t *tok_map,
-                int64_t S, int64_t H, int K, void *out, int out_dtype,
-                moe_stream_t stream);
+int moe_combine(const void *y, int64_t y_rows, int in_dtype, const float *topk_w,
+                const int64_t *tok_map, int64_t S, int64_t H, int K, void *out,
+                int out_dtype, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Dedup combine  [mori #448 StdMoE note: convert_combine_input per received

@@ -60,6 +60,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_e4m3_to_f32.restype = ctypes.c_float
     lib.oracle_plan.argtypes = [P, I64, I32, I32, P, P, P, P, P]
     lib.oracle_plan.restype = I32
+    lib.oracle_plan_capacity.argtypes = [P, I64, I32, I32, I64, P, P, P, P, P, P]
+    lib.oracle_plan_capacity.restype = I32
     lib.oracle_group_plan.argtypes = [P, P, I64, I32, I32, I32, P, P, P, P, P]
     lib.oracle_group_plan.restype = I32
     lib.oracle_dispatch.argtypes = [P, I64, I64, I32, P, P]
@@ -109,6 +111,25 @@ def plan(topk_idx: np.ndarray, E: int, lib=None):
     assert rc == 0
     return dict(cnt=cnt, off=off, packed_src=src[: int(off[E])], tok_map=tmap,
                 n_invalid=int(ninv[0]))
+
+
+def plan_capacity(topk_idx: np.ndarray, E: int, capacity: int, lib=None):
+    """Returns dict(cnt, off, packed_src i32[E*capacity] (unwritten rows -7),
+    tok_map, n_invalid, n_dropped)."""
+    lib = lib or load()
+    idx = _c(topk_idx, np.int32)
+    S, K = idx.shape
+    cnt = np.zeros(E, np.int32)
+    off = np.zeros(E + 1, np.int64)
+    src = np.full(max(E * capacity, 1), -7, np.int32)
+    tmap = np.zeros((S, K), np.int64)
+    ninv = np.zeros(1, np.int32)
+    ndrop = np.zeros(1, np.int32)
+    rc = lib.oracle_plan_capacity(_p(idx), S, K, E, capacity, _p(cnt), _p(off), _p(src),
+                                  _p(tmap), _p(ninv), _p(ndrop))
+    assert rc == 0
+    return dict(cnt=cnt, off=off, packed_src=src[:E * capacity], tok_map=tmap,
+                n_invalid=int(ninv[0]), n_dropped=int(ndrop[0]))
 
 
 def group_plan(topk_idx: np.ndarray, tok_map: np.ndarray, E: int, group_size: int, lib=None):

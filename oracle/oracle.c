@@ -211,6 +211,59 @@ ORACLE_API int oracle_plan(const int32_t *topk_idx, int64_t S, int K, int E,
 }
 
 /* ------------------------------------------------------------------------
+ * Plan with a per-expert capacity [mori448 op-parity note: receive slots are
+ * capped and over-cap tokens take the drop path, no out-of-bounds write].
+ * Reading for one GPU: each expert's bucket holds `capacity` rows, bucket e
+ * starts at row e*capacity; an entry keeps the slot it would get in the
+ * uncapped plan if that slot is below capacity, else it is dropped (-1).
+ *   cnt[e] = min(#{(s,k): idx == e}, capacity);  off[e] = e * capacity
+ *   tok_map[s,k] = e*capacity + slot if slot < capacity, else -1
+ *   packed_src[e*capacity + slot] = s*K + k for the kept entries
+ *   n_dropped = valid entries that did not fit
+ * ---------------------------------------------------------------------- */
+ORACLE_API int oracle_plan_capacity(const int32_t *topk_idx, int64_t S, int K, int E,
+                                    int64_t capacity, int32_t *cnt, int64_t *off,
+                                    int32_t *packed_src, int64_t *tok_map,
+                                    int32_t *n_invalid, int32_t *n_dropped)
+{
+    int32_t invalid = 0, dropped = 0;
+    int64_t *seen = (int64_t *)malloc(sizeof(int64_t) * (size_t)(E > 0 ? E : 1));
+    if (!seen)
+        return -1;
+    for (int e = 0; e < E; ++e)
+        seen[e] = 0;
+    for (int64_t s = 0; s < S; ++s) {
+        for (int k = 0; k < K; ++k) {
+            int64_t i = s * K + k;
+            int32_t e = topk_idx[i];
+            if (e < 0 || e >= E) {
+                tok_map[i] = -1;
+                invalid += 1;
+                continue;
+            }
+            int64_t slot = seen[e];
+            seen[e] += 1;
+            if (slot < capacity) {
+                tok_map[i] = e * capacity + slot;
+                packed_src[e * capacity + slot] = (int32_t)i;
+            } else {
+                tok_map[i] = -1;
+                dropped += 1;
+            }
+        }
+    }
+    for (int e = 0; e < E; ++e) {
+        cnt[e] = (int32_t)(seen[e] < capacity ? seen[e] : capacity);
+        off[e] = (int64_t)e * capacity;
+    }
+    off[E] = (int64_t)E * capacity;
+    free(seen);
+    *n_invalid = invalid;
+    *n_dropped = dropped;
+    return 0;
+}
+
+/* ------------------------------------------------------------------------
  * Dedup plan [mori448 PR description: ballot dedup sends a token once per
  * destination; StdMoE note: the receiver's i64 map holds -1 for the
  * token's experts that live elsewhere].  Groups play the destinations.

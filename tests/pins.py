@@ -420,6 +420,56 @@ def pin_expert_stages(lib):
     assert np.array_equal(y8, ref)
 
 
+def plan_capacity_by_sorting(idx: np.ndarray, E: int, cap: int):
+    """Second method: stable-sort the valid entries by expert; an entry's
+    rank in its expert is its sorted position minus the expert's first
+    position; ranks below cap keep row e*cap + rank."""
+    flat = idx.reshape(-1)
+    valid = (flat >= 0) & (flat < E)
+    ids = np.nonzero(valid)[0]
+    order = ids[np.argsort(flat[ids], kind="stable")]
+    ex = flat[order]
+    first = np.searchsorted(ex, ex, side="left")
+    rank = np.arange(order.size) - first
+    keep = rank < cap
+    tok_map = np.full(flat.shape, -1, np.int64)
+    tok_map[order[keep]] = ex[keep].astype(np.int64) * cap + rank[keep]
+    src = np.full(E * cap, -7, np.int32)
+    src[ex[keep].astype(np.int64) * cap + rank[keep]] = order[keep]
+    counts = np.bincount(flat[ids], minlength=E)
+    cnt = np.minimum(counts, cap).astype(np.int32)
+    off = (np.arange(E + 1) * cap).astype(np.int64)
+    return cnt, off, tok_map.reshape(idx.shape), src, int((~valid).sum()), int((counts - cnt).sum())
+
+
+def pin_plan_capacity_bruteforce(lib, S=2, K=2, E=3):
+    vals = list(range(-1, E + 1))
+    for cap in (1, 2, 3):
+        for combo in itertools.product(vals, repeat=S * K):
+            idx = np.array(combo, np.int32).reshape(S, K)
+            p = oracle.plan_capacity(idx, E, cap, lib=lib)
+            cnt, off, tmap, src, ninv, ndrop = plan_capacity_by_sorting(idx, E, cap)
+            assert np.array_equal(p["cnt"], cnt), (cap, combo)
+            assert np.array_equal(p["off"], off), (cap, combo)
+            assert np.array_equal(p["tok_map"], tmap), (cap, combo, p["tok_map"], tmap)
+            assert np.array_equal(p["packed_src"], src), (cap, combo)
+            assert p["n_invalid"] == ninv and p["n_dropped"] == ndrop, (cap, combo)
+
+
+def pin_plan_capacity_hand_example(lib):
+    """Worked by hand.  S=3, K=2, E=3, capacity 1:
+        token 0 -> (2, 0); token 1 -> (0, 2); token 2 -> (1, -1)
+    expert 0 keeps (0,1), drops (1,0); expert 1 keeps (2,0); expert 2 keeps
+    (0,0), drops (1,1).  Rows are e*1 + 0."""
+    idx = np.array([[2, 0], [0, 2], [1, -1]], np.int32)
+    p = oracle.plan_capacity(idx, 3, 1, lib=lib)
+    assert p["cnt"].tolist() == [1, 1, 1]
+    assert p["off"].tolist() == [0, 1, 2, 3]
+    assert p["tok_map"].tolist() == [[2, 0], [-1, -1], [1, -1]]
+    assert p["packed_src"].tolist() == [1, 4, 0]
+    assert p["n_invalid"] == 1 and p["n_dropped"] == 2
+
+
 def _e4m3_torch(vals: np.ndarray) -> np.ndarray:
     import torch
     return torch.from_numpy(np.ascontiguousarray(vals, np.float32)).to(
@@ -484,6 +534,7 @@ def pin_quant_fp8_rule(lib):
 
 ALL_PINS = [
     pin_plan_bruteforce, pin_plan_hand_example, pin_plan_invariants,
+    pin_plan_capacity_bruteforce, pin_plan_capacity_hand_example,
     pin_group_plan_bruteforce, pin_group_plan_invariants,
     pin_dispatch_scatter, pin_dispatch_dedup,
     pin_combine_exact_rational, pin_combine_identity_telescopes,

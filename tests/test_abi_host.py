@@ -74,12 +74,13 @@ def test_group_plan_rejects(L):
 def test_dispatch_validation(L):
     d = lambda **k: L.moe_dispatch(k.get("x", FAKE), k.get("S", 4), k.get("H", 64),
                                    k.get("dt", 0), k.get("K", 2), k.get("tm", FAKE),
-                                   k.get("px", FAKE), k.get("xs", None), k.get("ns", 0),
-                                   k.get("ps", None), None)
+                                   k.get("px", FAKE), k.get("rows", 8), k.get("xs", None),
+                                   k.get("ns", 0), k.get("ps", None), None)
     assert d(S=0) == OK                      # nothing to do, nothing enqueued
     assert d(dt=7) == EINVAL
     assert d(K=0) == EINVAL
     assert d(x=None) == EINVAL
+    assert d(rows=0) == EINVAL
     assert d(H=4) == EALIGN                  # 8-byte rows
     assert d(x=MIS) == EALIGN
     assert d(px=MIS) == EALIGN
@@ -92,13 +93,16 @@ def test_dispatch_validation(L):
 
 
 def test_combine_validation(L):
-    c = lambda **k: L.moe_combine(k.get("y", FAKE), k.get("idt", 0), k.get("w", FAKE),
-                                  k.get("tm", FAKE), k.get("S", 4), k.get("H", 64),
-                                  k.get("K", 2), k.get("out", FAKE), k.get("odt", 0), None)
+    c = lambda **k: L.moe_combine(k.get("y", FAKE), k.get("rows", 8), k.get("idt", 0),
+                                  k.get("w", FAKE), k.get("tm", FAKE), k.get("S", 4),
+                                  k.get("H", 64), k.get("K", 2), k.get("out", FAKE),
+                                  k.get("odt", 0), None)
     assert c(S=0) == OK
     assert c(idt=2) == EINVAL                # fp8 is a transport type, not a combine input
     assert c(odt=5) == EINVAL
     assert c(w=None) == EINVAL
+    assert c(rows=0) == EINVAL
+    assert c(rows=1 << 31) == EINVAL
     assert c(H=12) == EALIGN
     assert c(out=MIS) == EALIGN
     assert L.moe_combine_dedup(FAKE, 1, FAKE, FAKE, 8, FAKE, FAKE, FAKE, 16, 64, 8, 127, FAKE,
@@ -120,13 +124,25 @@ def test_device_errors_rejects_null(L):
 def test_quant_dispatch_validation(L):
     q = lambda **k: L.moe_dispatch_quant_fp8(k.get("x", FAKE), k.get("S", 4), k.get("H", 256),
                                              k.get("K", 2), k.get("tm", FAKE), k.get("block", 128),
-                                             k.get("q", FAKE), k.get("sc", FAKE), None)
+                                             k.get("q", FAKE), k.get("sc", FAKE),
+                                             k.get("rows", 8), None)
     assert q(S=0) == OK
     assert q(block=100) == EINVAL
     assert q(block=512) == EINVAL
     assert q(H=192) == EINVAL                 # not a multiple of the block
     assert q(K=0) == EINVAL
     assert q(tm=None) == EINVAL
+    assert q(rows=0) == EINVAL
     assert q(x=MIS) == EALIGN
     assert q(q=MIS) == EALIGN
     assert q(sc=FAKE + 2) == EALIGN
+
+
+def test_capacity_plan_validation(L):
+    c = lambda **k: L.moe_plan_capacity(FAKE, k.get("S", 16), 2, k.get("E", 8), k.get("cap", 4),
+                                        FAKE, FAKE, FAKE, FAKE, FAKE, k.get("nd", FAKE), None, 0,
+                                        None)
+    assert c(cap=0) == EINVAL
+    assert c(cap=1 << 30, E=8) == EINVAL      # E * capacity >= 2^31
+    assert c(nd=None) == EINVAL
+    assert c(S=-1) == EINVAL

@@ -1,0 +1,93 @@
+"""Plan with a per-expert capacity (padded buckets, over-capacity entries
+dropped to -1) and the dispatch / combine that run on its padded layout,
+against the CPU oracle: maps, counts and rows bit-exact, combine bitwise."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+from tests import gpu_path  # noqa: E402
+
+
+def _run(wl, idx, cap):
+    import combine_moe_plan_02_gb300 as moe
+    S, K, E, H = wl.S, wl.K, wl.E, wl.H
+    dev = torch.device("cuda")
+    rows = E * cap
+    out = moe.CapacityPlan(gpu_path.poisoned((E,), torch.int32),
+                           gpu_path.poisoned((E + 1,), torch.int64),
+                           gpu_path.poisoned((rows,), torch.int32),
+                           gpu_path.poisoned((S, K), torch.int64),
+                           gpu_path.poisoned((1,), torch.int32),
+                           gpu_path.poisoned((1,), torch.int32), cap)
+    t_idx = torch.from_numpy(np.ascontiguousarray(idx)).to(dev)
+    moe.moe_plan_capacity(t_idx, E, cap, out=out)
+    x = torch.from_numpy(wl.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    packed = gpu_path.poisoned((rows, H), torch.bfloat16)
+    moe.moe_dispatch(x, out.tok_map, packed_x=packed)
+    w = torch.from_numpy(wl.topk_w).to(dev)
+    comb = gpu_path.poisoned((S, H), torch.bfloat16)
+    moe.moe_combine(packed, w, out.tok_map, out=comb)
+    torch.cuda.synchronize()
+    assert moe.moe_device_errors() == 0
+    np_ = gpu_path._np
+    return dict(cnt=np_(out.cnt), off=np_(out.off), packed_src=np_(out.packed_src),
+                tok_map=np_(out.tok_map), n_invalid=int(out.n_invalid.item()),
+                n_dropped=int(out.n_dropped.item()), packed=np_(packed), out=np_(comb))
+
+
+def _check(wl, idx, cap):
+    res = _run(wl, idx, cap)
+    ref = oracle.plan_capacity(idx, wl.E, cap)
+    for key in ("cnt", "off", "tok_map"):
+        assert np.array_equal(res[key], ref[key]), key
+    assert res["n_invalid"] == ref["n_invalid"] and res["n_dropped"] == ref["n_dropped"]
+    rows = wl.E * cap
+    kept = np.zeros(rows, bool)
+    for e in range(wl.E):
+        kept[e * cap: e * cap + ref["cnt"][e]] = True
+    assert np.array_equal(res["packed_src"][kept], ref["packed_src"][kept])
+    assert np.all(res["packed_src"][~kept].view(np.uint32) == 0xFFFFFFFF)   # untouched
+    ref_packed = oracle.dispatch(wl.x, ref["tok_map"], rows)
+    assert np.array_equal(res["packed"][kept], ref_packed[kept])
+    assert np.all(res["packed"][~kept] == 0xFFFF)
+    ref_out = oracle.combine(ref_packed, "bf16", wl.topk_w, ref["tok_map"], wl.H, "bf16")
+    assert np.array_equal(res["out"], ref_out)
+    return res, ref
+
+
+@pytest.mark.timeout(600)
+@pytest.mark.parametrize("S,E,K,cap", [
+    (100, 8, 2, 1),          # single-tile plan, heavy dropping
+    (700, 16, 4, 150),       # one launch, some drops
+    (4096, 64, 8, 512),      # the MoonEP shape at its mean load: drops on busy experts
+    (4096, 64, 8, 4096),     # capacity above every count: nothing dropped
+    (20000, 64, 8, 1800),    # two-kernel plan
+])
+def test_capacity_uniform(S, E, K, cap):
+    wl = workloads.make("moonep", seed=S + cap, S=S, H=64, E=E, K=K)
+    res, ref = _check(wl, wl.topk_idx, cap)
+    if cap >= S:
+        assert ref["n_dropped"] == 0
+
+
+@pytest.mark.timeout(600)
+def test_capacity_zipf_drops_hot_experts():
+    wl = workloads.make("zipf", seed=4, S=8192, H=64)
+    cap = 8192 * 8 // 256 * 2          # twice the mean load
+    res, ref = _check(wl, wl.topk_idx, cap)
+    assert ref["n_dropped"] > 0 and (ref["cnt"] == cap).sum() >= 4
+
+
+@pytest.mark.timeout(600)
+def test_capacity_with_invalid_ids():
+    wl = workloads.make("moonep", seed=9, S=900, H=32, E=32, K=4)
+    idx = wl.topk_idx.copy()
+    idx[::4, 1] = -1
+    idx[::9, 3] = 99
+    _check(wl, idx, 60)

@@ -72,6 +72,10 @@ MUTANTS = [
      [pins.pin_expert_stages, pins.pin_combine_expert_scale_closed_form]),
     ("dequant_wrong_block", "scales[r * nb + j / block]", "scales[r * nb + j % nb]",
      [pins.pin_expert_stages]),
+    ("capacity_keeps_late_entries", "if (slot < capacity) {", "if (slot < capacity + (s > 0)) {",
+     [pins.pin_plan_capacity_bruteforce, pins.pin_plan_capacity_hand_example]),
+    ("capacity_cnt_uncapped", "cnt[e] = (int32_t)(seen[e] < capacity ? seen[e] : capacity);",
+     "cnt[e] = (int32_t)seen[e];", [pins.pin_plan_capacity_bruteforce]),
     ("e4m3_encode_ties_up", "code = (lo & 1) ? (uint8_t)(lo + 1) : lo;  /* tie: even mantissa */",
      "code = (uint8_t)(lo + 1);", [pins.pin_e4m3_encode]),
     ("e4m3_encode_overflow_to_nan", "if (a >= 448.0)\n        return (uint8_t)(sign | 0x7e);",
