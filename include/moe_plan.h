@@ -34,9 +34,9 @@
  *     (1..32), E = experts (1..1024), H = elements per row.
  *   - Return value: MOE_OK, or an error code.  MOE_EINVAL / MOE_EALIGN are
  *     detected on the host before anything is enqueued.  MOE_ECUDA means a
- *     CUDA call failed; moe_last_cuda_error() returns its error code.  Data-dependent problems are never
- *     clamped: an expert id outside [0, E) is counted in *n_invalid and its
- *     entries are marked -1.
+ *     CUDA call failed; moe_last_cuda_error() returns its error code.
+ *     Data-dependent problems are never clamped: an expert id outside
+ *     [0, E) is counted in *n_invalid and its entries are marked -1.
  *   - S = 0 is valid: moe_plan still writes zero counts/offsets; the other
  *     calls enqueue nothing.
  */

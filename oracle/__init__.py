@@ -72,6 +72,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_combine.restype = None
     lib.oracle_combine_dedup.argtypes = [P, I32, P, I64, P, P, P, I64, I64, I32, P, P, I32]
     lib.oracle_combine_dedup.restype = None
+    lib.oracle_combine_fold.argtypes = [P, I32, P, I32, P, I64, I64, I32, P, I32, P]
+    lib.oracle_combine_fold.restype = None
     lib.oracle_expert_scale_bf16.argtypes = [P, P, I32, P, I64, P]
     lib.oracle_expert_scale_bf16.restype = None
     lib.oracle_expert_dequant_fp8.argtypes = [P, P, I64, I64, I32, P]
@@ -218,6 +220,22 @@ def combine_dedup(y: np.ndarray, in_dt: str, topk_w: np.ndarray, grp_src: np.nda
                              _p(gs) if R else None, _p(gtk) if R else None, _p(gtm), S, H, K,
                              _p(gtok), _p(out), _DT[out_dt])
     return gtok[:R], out
+
+
+def combine_fold(y: np.ndarray, in_dt: str, topk_w: np.ndarray, token_map: np.ndarray,
+                 H: int, out_dt: str, weighted: bool = False, fold: bool = True, lib=None):
+    """Combine over any token map, weighted or not, with the weight fold.
+    Returns (out, out_weights or None)."""
+    lib = lib or load()
+    y = _c(y, _np_dt(in_dt))
+    w = _c(topk_w, np.float32)
+    tm = _c(token_map, np.int64)
+    S, K = tm.shape
+    out = np.zeros((S, H), _np_dt(out_dt))
+    ow = np.zeros((S, K), np.float32) if fold else None
+    lib.oracle_combine_fold(_p(y) if y.size else None, _DT[in_dt], _p(w), int(weighted), _p(tm),
+                            S, H, K, _p(out), _DT[out_dt], _p(ow) if fold else None)
+    return out, ow
 
 
 def expert_scale_bf16(packed: np.ndarray, off: np.ndarray, c: np.ndarray, lib=None):

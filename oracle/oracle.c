@@ -464,6 +464,48 @@ ORACLE_API void oracle_combine_dedup(const void *y, int in_dt, const float *w,
 }
 
 /* ------------------------------------------------------------------------
+ * Combine with the weight fold [mori448 "Combine now reduces the K forwarded
+ * per-token weight vectors" note, and the op note whose identity round trip
+ * checks comb == U*input and out_weights == U*wts].  The token's whole weight
+ * vector travels with every copy of its row; the combine sums the copies it
+ * gathers, and folds the travelling weight vectors the same way:
+ *   out[s,j] = round( sum_{k : map[s,k] >= 0} c_k * y[map[s,k], j] )
+ *              with c_k = w[s,k] when `weighted`, else no factor at all;
+ *   ow[s,i]  = sum_{k : map[s,k] >= 0} w[s,i]
+ * both in f32, in increasing k.  `map` is any token map into y: tok_map over
+ * packed rows, or gtok_map over group rows (one copy per destination group),
+ * for which identity rows give out = U*x and ow = U*w, U being the number
+ * of the token's groups.  ow may be NULL (no fold).
+ * ---------------------------------------------------------------------- */
+ORACLE_API void oracle_combine_fold(const void *y, int in_dt, const float *w, int weighted,
+                                    const int64_t *map, int64_t S, int64_t H, int K,
+                                    void *out, int out_dt, float *ow)
+{
+    for (int64_t s = 0; s < S; ++s)
+        for (int64_t j = 0; j < H; ++j) {
+            float acc = 0.0f;
+            for (int k = 0; k < K; ++k) {
+                int64_t row = map[s * K + k];
+                if (row < 0)
+                    continue;
+                float v = load_elem(y, in_dt, row * H + j);
+                acc = acc + (weighted ? w[s * K + k] * v : v);
+            }
+            store_elem(out, out_dt, s * H + j, acc);
+        }
+    if (!ow)
+        return;
+    for (int64_t s = 0; s < S; ++s)
+        for (int i = 0; i < K; ++i) {
+            float acc = 0.0f;
+            for (int k = 0; k < K; ++k)
+                if (map[s * K + k] >= 0)
+                    acc = acc + w[s * K + i];
+            ow[s * K + i] = acc;
+        }
+}
+
+/* ------------------------------------------------------------------------
  * Synthetic expert stages (harness steps between dispatch and combine; not
  * part of the method, but the oracle runs its own copy so that no input of
  * its combine comes from the GPU).

@@ -363,6 +363,87 @@ def pin_combine_dedup_closed_forms(lib):
     assert np.all(np.abs(out1 - exact1) <= 4 * wl.K * U_F32 * (U[:, None] * np.abs(xs)) + 1e-30)
 
 
+def _group_rows_setup(lib, seed, S, H, E=64, K=8, gs=8):
+    """bf16 MoonEP-like routing, its group plan, and the group-row copies of x."""
+    import workloads
+    wl = workloads.make("moonep", seed=seed, S=S, H=H, E=E, K=K)
+    p = oracle.plan(wl.topk_idx, wl.E, lib=lib)
+    gp = oracle.group_plan(wl.topk_idx, p["tok_map"], wl.E, gs, lib=lib)
+    grp_x, _ = oracle.dispatch_dedup(wl.x, gp["grp_src"], gp["grp_tok_map"], wl.K,
+                                     int(p["off"][-1]), lib=lib)
+    U = np.array([len(set((r // gs).tolist())) for r in wl.topk_idx], np.float64)
+    return wl, p, gp, grp_x, U
+
+
+def _dyadic_weights(seed, S, K):
+    """Weights m/256 with m in 1..255: at most 8 significant bits, so that up
+    to 8 repeated f32 additions stay exact."""
+    import workloads
+    m = np.floor(workloads.uniform01(seed, 60, S * K) * 255.0) + 1.0
+    return (m / 256.0).astype(np.float32).reshape(S, K)
+
+
+def pin_combine_fold_group_rows(lib):
+    """Unweighted combine over group rows with the weight fold (mori #448
+    op note: an identity round trip gives comb == U*input and
+    out_weights == U*wts, U = the token's distinct destinations).  With bf16
+    x and U <= 8 the f32 sum U*x is exact, so out == bf16(U*x) exactly
+    (bf16 rounding by torch's CPU cast); with 8-bit weights U*w is exact."""
+    import torch
+    wl, p, gp, grp_x, U = _group_rows_setup(lib, seed=21, S=48, H=32)
+    w = _dyadic_weights(21, wl.S, wl.K)
+    out, ow = oracle.combine_fold(grp_x, "bf16", w, gp["gtok_map"], wl.H, "bf16",
+                                  weighted=False, lib=lib)
+    ux = (U[:, None] * bf16_bits_to_f64(wl.x)).astype(np.float32)
+    want = torch.from_numpy(ux).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(bf16_bits_to_f64(out), bf16_bits_to_f64(want))
+    assert np.array_equal(ow.astype(np.float64), U[:, None] * w.astype(np.float64))
+    # softmax weights: U*w up to the rounding of U-1 additions
+    ws = wl.topk_w.astype(np.float64)
+    _, ow2 = oracle.combine_fold(grp_x, "bf16", wl.topk_w, gp["gtok_map"], wl.H, "bf16",
+                                 weighted=False, lib=lib)
+    gam = (U * U_F32 / (1 - U * U_F32))[:, None]
+    assert np.all(np.abs(ow2 - U[:, None] * ws) <= gam * U[:, None] * ws)
+
+
+def pin_combine_fold_direct_map(lib):
+    """Fold over the per-expert token map: every valid entry forwards the
+    token's whole weight vector, so out_weights[s] == V[s] * w[s] with V the
+    valid entries (unused entries drop out); the unweighted rows give V*x."""
+    import workloads
+    wl = workloads.make("tiny", seed=22, K=4)
+    idx = wl.topk_idx.copy()
+    idx[1, 0] = -1
+    idx[5, :3] = wl.E
+    idx[9, :] = -1
+    p = oracle.plan(idx, wl.E, lib=lib)
+    packed = oracle.dispatch(wl.x, p["tok_map"], max(int(p["off"][-1]), 1), lib=lib)
+    w = _dyadic_weights(22, wl.S, wl.K)
+    out, ow = oracle.combine_fold(packed, "bf16", w, p["tok_map"], wl.H, "f32",
+                                  weighted=False, lib=lib)
+    V = (p["tok_map"] >= 0).sum(axis=1).astype(np.float64)
+    assert V[9] == 0 and V[5] == 1 and V[1] == 3
+    assert np.array_equal(ow.astype(np.float64), V[:, None] * w.astype(np.float64))
+    assert np.array_equal(out.astype(np.float64), V[:, None] * bf16_bits_to_f64(wl.x))
+
+
+def pin_combine_fold_weighted_telescopes(lib):
+    """Weighted mode of the fold combine is the StdMoE combine: identity
+    experts give (sum over valid k of w) * x within the rounding bound."""
+    import workloads
+    wl = workloads.make("tiny", seed=23)
+    p = oracle.plan(wl.topk_idx, wl.E, lib=lib)
+    packed = oracle.dispatch(wl.x, p["tok_map"], int(p["off"][-1]), lib=lib)
+    out, ow = oracle.combine_fold(packed, "bf16", wl.topk_w, p["tok_map"], wl.H, "bf16",
+                                  weighted=True, fold=False, lib=lib)
+    assert ow is None
+    xs = bf16_bits_to_f64(wl.x)
+    wsum = wl.topk_w.astype(np.float64).sum(axis=1)
+    exact = wsum[:, None] * xs
+    bound = combine_error_bound(wsum[:, None] * np.abs(xs), exact, wl.K, True)
+    assert np.all(np.abs(bf16_bits_to_f64(out) - exact) <= bound)
+
+
 # ---------------------------------------------------------------------------
 # number formats and expert stages, against torch's CPU conversions
 # ---------------------------------------------------------------------------
@@ -540,5 +621,6 @@ ALL_PINS = [
     pin_combine_exact_rational, pin_combine_identity_telescopes,
     pin_combine_expert_scale_closed_form, pin_combine_single_k_is_copy, pin_combine_k_order,
     pin_combine_dedup_closed_forms,
+    pin_combine_fold_group_rows, pin_combine_fold_direct_map, pin_combine_fold_weighted_telescopes,
     pin_bf16_rounding, pin_e4m3_table, pin_expert_stages, pin_e4m3_encode, pin_quant_fp8_rule,
 ]

@@ -63,6 +63,16 @@ MUTANTS = [
      [pins.pin_combine_identity_telescopes, pins.pin_combine_exact_rational]),
     ("dedup_stage2_weighted", "acc = acc + gtok[r * H + j];", "acc = acc + w[s * K + k] * gtok[r * H + j];",
      [pins.pin_combine_dedup_closed_forms]),
+    ("fold_counts_unused_entries", "if (map[s * K + k] >= 0)\n                    acc = acc + w[s * K + i];",
+     "if (map[s * K + k] >= -1)\n                    acc = acc + w[s * K + i];",
+     [pins.pin_combine_fold_direct_map]),
+    ("fold_sums_other_weights", "acc = acc + w[s * K + i];", "acc = acc + w[s * K + k];",
+     [pins.pin_combine_fold_group_rows, pins.pin_combine_fold_direct_map]),
+    ("fold_unweighted_still_weights", "acc = acc + (weighted ? w[s * K + k] * v : v);",
+     "acc = acc + w[s * K + k] * v;",
+     [pins.pin_combine_fold_group_rows, pins.pin_combine_fold_direct_map]),
+    ("fold_weighted_ignores_weights", "acc = acc + (weighted ? w[s * K + k] * v : v);",
+     "acc = acc + v;", [pins.pin_combine_fold_weighted_telescopes]),
     ("bf16_ties_away", "if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u)))",
      "if (rest >= 0x8000u)", [pins.pin_bf16_rounding]),
     ("bf16_truncates", "keep += 1u;", ";", [pins.pin_bf16_rounding, pins.pin_combine_exact_rational]),
