@@ -21,7 +21,7 @@ from ._abi import MoeError, MOE_BF16, MOE_F32, MOE_FP8_E4M3  # noqa: F401
 
 __all__ = [
     "moe_plan", "moe_group_plan", "moe_dispatch", "moe_dispatch_dedup", "moe_dispatch_quant_fp8",
-    "moe_combine",
+    "moe_combine", "moe_combine_fold",
     "moe_combine_dedup", "moe_plan_workspace_size", "moe_group_plan_workspace_size",
     "moe_device_errors", "moe_plan_capacity", "Plan", "GroupPlan", "CapacityPlan", "MoeError",
     "lib",
@@ -273,6 +273,28 @@ def moe_combine_dedup(y: torch.Tensor, topk_w: torch.Tensor, gp: GroupPlan, *,
         _ptr(gp.grp_tok_map), _ptr(gp.gtok_map), S, H, K, gp.max_rows, _ptr(gtok), _ptr(out),
         _dt(out), _stream(stream)))
     return gtok, out
+
+
+def moe_combine_fold(y: torch.Tensor, topk_w: Optional[torch.Tensor], token_map: torch.Tensor,
+                     *, weighted: bool = False, fold: bool = True,
+                     out_dtype: torch.dtype = torch.bfloat16, out: Optional[torch.Tensor] = None,
+                     out_weights: Optional[torch.Tensor] = None, stream=None):
+    """out[s] = sum over valid k of (topk_w[s,k] if weighted else 1) *
+    y[token_map[s,k]]; out_weights[s,i] = sum over valid k of topk_w[s,i].
+    token_map is tok_map (packed rows) or gtok_map (group rows).
+    Returns (out, out_weights or None)."""
+    S, K = token_map.shape
+    H = y.shape[1]
+    if out is None:
+        out = torch.empty(S, H, dtype=out_dtype, device=y.device)
+    if fold and out_weights is None:
+        out_weights = torch.empty(S, K, dtype=torch.float32, device=y.device)
+    if not fold:
+        out_weights = None
+    _abi.check("moe_combine_fold", lib().moe_combine_fold(
+        _ptr(y), y.shape[0], _dt(y), _ptr(topk_w), int(weighted), _ptr(token_map), S, H, K,
+        _ptr(out), _dt(out), _ptr(out_weights), _stream(stream)))
+    return out, out_weights
 
 
 def moe_device_errors() -> int:

@@ -34,6 +34,7 @@ SIGNATURES = {
     "moe_dispatch_quant_fp8": (I32, [P, I64, I64, I32, P, I32, P, P, I64, P]),
     "moe_combine": (I32, [P, I64, I32, P, P, I64, I64, I32, P, I32, P]),
     "moe_combine_dedup": (I32, [P, I32, P, P, I32, P, P, P, I64, I64, I32, I64, P, P, I32, P]),
+    "moe_combine_fold": (I32, [P, I64, I32, P, I32, P, I64, I64, I32, P, I32, P, P]),
     "moe_device_errors": (I32, [P]),
 }
 

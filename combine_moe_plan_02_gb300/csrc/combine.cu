@@ -16,6 +16,12 @@
 // separately rounded multiply and add, and stores the rounded result with
 // one 16-byte store.  A persistent grid sized to the SM count strides over
 // units.  There is no shared memory, no atomics and no inter-CTA wait.
+//
+// Weight fold (mori #448, the note on reducing the K forwarded per-token
+// weight vectors into out_weights, folded into the gather at part 0): the
+// warp that owns slice 0 of a row also writes out_weights[row, j], the sum of
+// w[row, j] over the row's valid copies, from the map entries it already
+// holds.
 
 #include "common.cuh"
 
@@ -50,6 +56,7 @@ struct CombineArgs {
     int R;                     // steps per lane per unit
     int slices;                // units per row
     uint8_t *out;
+    float *out_w;              // if set: [rows, K] weight fold (reads w[i, *])
 };
 
 template <typename T> struct Io;
@@ -142,6 +149,17 @@ __global__ void __launch_bounds__(kThreads, MOE_COMBINE_MIN_BLOCKS) combine_kern
                 my_row = -1;
             } else if (WM != kUnweighted && my_row >= 0) {
                 my_w = __ldg(a.w + wr * K + lane);
+            }
+        }
+        if (a.out_w != nullptr && sl == 0) {
+            // weight fold: the token's weight vector travels with each of its
+            // valid copies, so entry j accumulates w[i, j] once per copy
+            const unsigned valid = __ballot_sync(0xffffffffu, lane < K && my_row >= 0);
+            if (lane < K) {
+                const float fw = __ldg(a.w + i * K + lane);
+                float acc = 0.0f;
+                for (int c = __popc(valid); c > 0; --c) acc = __fadd_rn(acc, fw);
+                a.out_w[i * K + lane] = acc;
             }
         }
         const int64_t pbase = (int64_t)sl * 32 * a.R;
@@ -307,6 +325,33 @@ MOE_EXPORT int moe_combine_dedup(const void *y, int in_dtype, const float *topk_
     b.steps = H / 8;
     b.out = static_cast<uint8_t *>(out);
     return launch_combine(b, MOE_F32, out_dtype, kUnweighted, (cudaStream_t)stream);
+}
+
+MOE_EXPORT int moe_combine_fold(const void *y, int64_t y_rows, int in_dtype,
+                                const float *topk_w, int weighted, const int64_t *map, int64_t S,
+                                int64_t H, int K, void *out, int out_dtype, float *out_weights,
+                                moe_stream_t stream)
+{
+    if (!combine_dtype_ok(in_dtype) || !combine_dtype_ok(out_dtype)) return MOE_EINVAL;
+    if (S < 0 || H < 1 || K < 1 || K > 32 || (weighted != 0 && weighted != 1)) return MOE_EINVAL;
+    if (S == 0) return MOE_OK;
+    if (!y || !map || !out || y_rows < 1 || y_rows >= ((int64_t)1 << 31)) return MOE_EINVAL;
+    if ((weighted || out_weights) && !topk_w) return MOE_EINVAL;
+    if (H % 8 || !aligned16(y) || !aligned16(out)) return MOE_EALIGN;
+    if (out_weights && (reinterpret_cast<uintptr_t>(out_weights) & 3)) return MOE_EALIGN;
+    CombineArgs a = {};
+    a.y = static_cast<const uint8_t *>(y);
+    a.w = topk_w;
+    a.map = map;
+    a.rows = S;
+    a.y_rows = y_rows;
+    a.K = K;
+    a.H = H;
+    a.steps = H / 8;
+    a.out = static_cast<uint8_t *>(out);
+    a.out_w = out_weights;
+    return launch_combine(a, in_dtype, out_dtype, weighted ? kWeightDirect : kUnweighted,
+                          (cudaStream_t)stream);
 }
 
 namespace moe {

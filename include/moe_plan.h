@@ -7,6 +7,8 @@
  *   moe_dispatch  scatter each token row into its K per-expert buckets
  *   (expert computation by the caller: packed rows -> expert output rows y)
  *   moe_combine   gather each token's K output rows, weighted f32 sum
+ *                 (moe_combine_fold: unweighted or weighted, with the sum
+ *                 of the forwarded weight vectors)
  * with a dedup variant (moe_group_plan, moe_dispatch_dedup,
  * moe_combine_dedup) that sends each token once per virtual expert group and
  * expands per expert from there.
@@ -291,6 +293,36 @@ int moe_combine_dedup(const void *y, int in_dtype, const float *topk_w,
                       const int64_t *grp_tok_map, const int64_t *gtok_map, int64_t S,
                       int64_t H, int K, int64_t max_rows, float *gtok, void *out,
                       int out_dtype, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Combine with the weight fold  [mori #448: the combine-weight-fold note (the
+ * K per-token weight vectors forwarded with the copies are reduced into
+ * out_weights, once per token in the gather's first part) and the op note
+ * (identity round trip: comb == U*input, out_weights == U*wts, U = the
+ * token's distinct destinations); mori EPv2 v2-native note (same golden)].
+ *
+ *   out[s, j]         = round_out( sum over k with map[s,k] >= 0 of
+ *                                  c_k * y[map[s,k], j] )
+ *                       c_k = topk_w[s,k] if weighted == 1; no factor if 0
+ *   out_weights[s, i] = sum over k with map[s,k] >= 0 of topk_w[s, i]
+ * Both sums in f32, increasing k, separately rounded; bf16 output rounds to
+ * nearest even.  weighted == 1 with out_weights == NULL is moe_combine.
+ *
+ * map     int64 [S, K]: any token map into y -- tok_map from moe_plan (rows
+ *         of y = expert outputs in packed order) or gtok_map from
+ *         moe_group_plan (rows of y = one output row per (token, group),
+ *         e.g. the group rows of moe_dispatch_dedup after a per-group stage)
+ * y       [y_rows, H] of in_dtype (MOE_BF16 or MOE_F32), 1 <= y_rows < 2^31;
+ *         an entry at or past y_rows drops its term and is flagged (bit 2)
+ * topk_w  f32 [S, K]; may be NULL only when weighted == 0 and
+ *         out_weights == NULL
+ * out     [S, H] of out_dtype; out_weights f32 [S, K] (4-byte aligned) or
+ *         NULL for no fold
+ * Alignment as moe_combine.  weighted other than 0 or 1 is MOE_EINVAL.
+ * ---------------------------------------------------------------------- */
+int moe_combine_fold(const void *y, int64_t y_rows, int in_dtype, const float *topk_w,
+                     int weighted, const int64_t *map, int64_t S, int64_t H, int K,
+                     void *out, int out_dtype, float *out_weights, moe_stream_t stream);
 
 #ifdef __cplusplus
 }

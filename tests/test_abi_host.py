@@ -109,6 +109,24 @@ def test_combine_validation(L):
                                FAKE, 1, None) == EINVAL
 
 
+def test_combine_fold_validation(L):
+    c = lambda **k: L.moe_combine_fold(k.get("y", FAKE), k.get("rows", 8), k.get("idt", 0),
+                                       k.get("w", FAKE), k.get("wt", 0), k.get("tm", FAKE),
+                                       k.get("S", 4), k.get("H", 64), k.get("K", 2),
+                                       k.get("out", FAKE), k.get("odt", 0), k.get("ow", FAKE),
+                                       None)
+    assert c(S=0) == OK
+    assert c(wt=2) == EINVAL                 # weighted is 0 or 1
+    assert c(w=None) == EINVAL               # the fold needs the weights
+    assert c(w=None, wt=1, ow=None) == EINVAL
+    assert c(idt=2) == EINVAL
+    assert c(K=33) == EINVAL
+    assert c(tm=None) == EINVAL
+    assert c(ow=FAKE + 2) == EALIGN
+    assert c(H=12) == EALIGN
+    assert c(y=MIS) == EALIGN
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_abi, "_lib", None)
     monkeypatch.setattr(_abi, "LIB_PATH", str(tmp_path / "missing.so"))
