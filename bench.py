@@ -252,7 +252,8 @@ def small_token_latency(dev, reps: int = 50):
     res = {"workload": "fp8small: H=6144 E=256 K=8, fp8 e4m3 rows + 48 f32 scales per row, "
                        "bf16 expert outputs, bf16 combine; inputs resident, y precomputed",
            "S": [], "eager_us": [], "graph_us": [], "plan_us": [], "dispatch_us": [],
-           "combine_us": []}
+           "combine_us": [], "fused_eager_us": [], "fused_graph_us": [],
+           "plan_dispatch_us": [], "fused_max_entries": None}
     stream = torch.cuda.Stream(dev)  # graphs are captured on a non-default stream
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(stream):
@@ -314,7 +315,49 @@ def _small_token_sweep(moe, torch, dev, stream, reps, res):
             g.replay()
             b.record(stream)
         torch.cuda.synchronize()
+        # moe_plan_dispatch (one launch up to the crossover) + combine
+        def calls_fused():
+            moe.moe_plan_dispatch(idx, x, E, x_scales=xs, out=plan, packed_x=px,
+                                  packed_scales=ps, stream=stream)
+            moe.moe_combine(y, w, plan.tok_map, out=out, stream=stream)
+
+        for _ in range(10):
+            calls_fused()
+        torch.cuda.synchronize()
+        f_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+        for e in f_ev:
+            e[0].record(stream)
+            moe.moe_plan_dispatch(idx, x, E, x_scales=xs, out=plan, packed_x=px,
+                                  packed_scales=ps, stream=stream)
+            e[1].record(stream)
+            moe.moe_combine(y, w, plan.tok_map, out=out, stream=stream)
+            e[2].record(stream)
+        torch.cuda.synchronize()
+        fs_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(reps)]
+        for a, b in fs_ev:
+            a.record(stream)
+            calls_fused()
+            b.record(stream)
+        torch.cuda.synchronize()
+        gf = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gf, stream=stream):
+            calls_fused()
+        for _ in range(5):
+            gf.replay()
+        torch.cuda.synchronize()
+        gf_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(reps)]
+        for a, b in gf_ev:
+            a.record(stream)
+            gf.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
         med = lambda xs_: round(1e3 * statistics.median(xs_), 2)
+        res["fused_eager_us"].append(med([a.elapsed_time(b) for a, b in fs_ev]))
+        res["plan_dispatch_us"].append(med([e[0].elapsed_time(e[1]) for e in f_ev]))
+        res["fused_graph_us"].append(med([a.elapsed_time(b) for a, b in gf_ev]))
+        res["fused_max_entries"] = int(moe.lib().moe_plan_dispatch_fused_max())
         res["S"].append(S)
         res["eager_us"].append(med([a.elapsed_time(b) for a, b in step_ev]))
         res["graph_us"].append(med([a.elapsed_time(b) for a, b in g_ev]))

@@ -20,7 +20,7 @@ from . import _abi
 from ._abi import MoeError, MOE_BF16, MOE_F32, MOE_FP8_E4M3  # noqa: F401
 
 __all__ = [
-    "moe_plan", "moe_group_plan", "moe_dispatch", "moe_dispatch_dedup", "moe_dispatch_quant_fp8",
+    "moe_plan", "moe_group_plan", "moe_dispatch", "moe_plan_dispatch", "moe_dispatch_dedup", "moe_dispatch_quant_fp8",
     "moe_combine", "moe_combine_fold",
     "moe_combine_dedup", "moe_plan_workspace_size", "moe_group_plan_workspace_size",
     "moe_device_errors", "moe_plan_capacity", "Plan", "GroupPlan", "CapacityPlan", "MoeError",
@@ -205,6 +205,46 @@ def moe_dispatch(x: torch.Tensor, tok_map: torch.Tensor, *, packed_x: Optional[t
         _ptr(x), S, H, _dt(x), K, _ptr(tok_map), _ptr(packed_x), packed_x.shape[0],
         _ptr(x_scales), n_scales, _ptr(packed_scales), _stream(stream)))
     return packed_x, packed_scales
+
+
+def moe_plan_dispatch(topk_idx: torch.Tensor, x: torch.Tensor, E: int, *,
+                      x_scales: Optional[torch.Tensor] = None, out: Optional[Plan] = None,
+                      packed_x: Optional[torch.Tensor] = None,
+                      packed_scales: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None, stream=None):
+    """moe_plan followed by moe_dispatch, in one launch for small batches.
+    Returns (plan, packed_x, packed_scales)."""
+    if topk_idx.dtype != torch.int32 or topk_idx.dim() != 2:
+        raise TypeError("topk_idx must be int32 [S, K]")
+    S, K = topk_idx.shape
+    H = x.shape[1]
+    dev = topk_idx.device
+    if out is None:
+        out = Plan(torch.empty(E, dtype=torch.int32, device=dev),
+                   torch.empty(E + 1, dtype=torch.int64, device=dev),
+                   torch.empty(max(S * K, 1), dtype=torch.int32, device=dev),
+                   torch.empty(S, K, dtype=torch.int64, device=dev),
+                   torch.empty(1, dtype=torch.int32, device=dev))
+    if packed_x is None:
+        packed_x = torch.empty(max(S * K, 1), H, dtype=x.dtype, device=dev)
+    n_scales = 0
+    if x_scales is not None:
+        n_scales = x_scales.shape[1]
+        if packed_scales is None:
+            packed_scales = torch.empty(packed_x.shape[0], n_scales, dtype=torch.float32,
+                                        device=dev)
+    if packed_scales is not None and packed_scales.shape[0] < packed_x.shape[0]:
+        raise ValueError("packed_scales needs as many rows as packed_x")
+    L = lib()
+    nws = 0
+    if S * K > int(L.moe_plan_dispatch_fused_max()):
+        nws = int(L.moe_plan_workspace_size(S, K, E))
+    ws = _workspace(nws, dev, workspace)
+    _abi.check("moe_plan_dispatch", L.moe_plan_dispatch(
+        _ptr(topk_idx), _ptr(x), S, H, _dt(x), K, E, _ptr(x_scales), n_scales, _ptr(out.cnt),
+        _ptr(out.off), _ptr(out.packed_src), _ptr(out.tok_map), _ptr(out.n_invalid),
+        _ptr(packed_x), packed_x.shape[0], _ptr(packed_scales), _ptr(ws), nws, _stream(stream)))
+    return out, packed_x, packed_scales
 
 
 def moe_dispatch_quant_fp8(x: torch.Tensor, tok_map: torch.Tensor, *, block: int = 128,

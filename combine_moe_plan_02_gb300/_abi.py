@@ -35,6 +35,9 @@ SIGNATURES = {
     "moe_combine": (I32, [P, I64, I32, P, P, I64, I64, I32, P, I32, P]),
     "moe_combine_dedup": (I32, [P, I32, P, P, I32, P, P, P, I64, I64, I32, I64, P, P, I32, P]),
     "moe_combine_fold": (I32, [P, I64, I32, P, I32, P, I64, I64, I32, P, I32, P, P]),
+    "moe_plan_dispatch_fused_max": (I64, []),
+    "moe_plan_dispatch": (I32, [P, P, I64, I64, I32, I32, I32, P, I64, P, P, P, P, P, P, I64, P,
+                                P, SZ, P]),
     "moe_device_errors": (I32, [P]),
 }
 

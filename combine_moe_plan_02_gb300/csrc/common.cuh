@@ -49,6 +49,7 @@ enum : uint32_t {
 };
 cudaError_t read_dispatch_errors(uint32_t *flags);
 cudaError_t read_combine_errors(uint32_t *flags);
+cudaError_t read_plan_dispatch_errors(uint32_t *flags);
 
 // Number of SMs of the current device (cached per device ordinal).
 int sm_count();

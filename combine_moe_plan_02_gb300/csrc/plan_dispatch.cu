@@ -1,0 +1,295 @@
+// Plan and dispatch in one launch for small batches.
+//
+// Sources: ROCm/mori "EPv2 internode dispatch/combine over CCO/GDA": the
+// page keeps two kernel families, a throughput one and a low-latency one,
+// and picks per call by token count (its automatic crossover sits at 512
+// tokens); ROCm/mori "Draft: cco + flydsl dispatch/combine #448", StdMoE note
+// (the plan outputs: per-expert counts, packed_src, the i64 slot map with -1)
+// and PR description (each token row is written once per destination).
+//
+// GB300 design: at small batch sizes a step is a chain of short kernels
+// whose cost is launch and tail latency, not bytes, so plan and dispatch are
+// fused.  Below the crossover the flat entry list holds at most
+// kFusedMaxEntries entries, few enough that every CTA of the launch ranks all
+// of them itself in shared memory -- the same stable (token, k) ranks as
+// moe_plan: per-warp counts by __match_any_sync, totals, an exclusive scan
+// over experts, a scan over warps per expert, then rank = expert offset +
+// warp base + running count + popc(peers below the lane).  CTA 0 also writes
+// the plan outputs.  Then every warp of the grid copies 512-byte segments of
+// token rows (32 lanes x 16 bytes) to the token's destinations, read from
+// the CTA's own copy of the map.  No CTA waits for another CTA.
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 1024;  // one expert per thread in the scan: E <= 1024
+constexpr int kWarps = kThreads / 32;
+constexpr int kSeg = 512;       // bytes of a row segment copied by one warp
+#ifndef MOE_PLAN_DISPATCH_FUSED_MAX
+#define MOE_PLAN_DISPATCH_FUSED_MAX 1024
+#endif
+constexpr int64_t kFusedMaxEntries = MOE_PLAN_DISPATCH_FUSED_MAX;
+
+__device__ uint32_t g_pd_error;  // kErrDispatchIndex
+
+struct PDArgs {
+    const int32_t *idx;   // [S, K]
+    int64_t S;
+    int K, E;
+    int64_t n;            // S * K
+    const uint8_t *x;     // [S, row_bytes]
+    int64_t row_bytes;
+    const uint8_t *xs;    // [S, scale_bytes] or null
+    int64_t scale_bytes;
+    int64_t segs, ssegs;  // 512-byte segments of a row / of a scale row
+    int32_t *cnt;         // [E]
+    int64_t *off;         // [E + 1]
+    int32_t *src;         // [n]
+    int64_t *map;         // [n]
+    int32_t *n_invalid;   // [1]
+    uint8_t *px;          // [packed_rows, row_bytes]
+    uint8_t *ps;          // [packed_rows, scale_bytes] or null
+    int64_t packed_rows;
+};
+
+// Exclusive scan of v over the block; sets `total`.
+__device__ __forceinline__ int32_t block_scan(int32_t v, int32_t *s_warp, int32_t &total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int32_t x = v;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int32_t w = s_warp[lane];
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        s_warp[lane] = w;
+    }
+    __syncthreads();
+    total = s_warp[kWarps - 1];
+    return (warp ? s_warp[warp - 1] : 0) + x - v;
+}
+
+// Expert of entry i, -1 if it takes no slot, -2 past the warp's range.
+__device__ __forceinline__ int entry_key(const PDArgs &a, int64_t i, bool in_range)
+{
+    if (!in_range) return -2;
+    const int e = __ldg(a.idx + i);
+    return (e >= 0 && e < a.E) ? e : -1;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) plan_dispatch_kernel(PDArgs a)
+{
+    extern __shared__ int32_t smem[];
+    const int wstride = a.E | 1;                 // odd: the column walks hit 32 banks
+    int32_t *s_wc = smem;                        // [kWarps][wstride] per-warp counts
+    int32_t *s_off = s_wc + kWarps * wstride;    // [E] bucket offsets
+    int32_t *s_row = s_off + a.E;                // [n] packed row of each entry
+    __shared__ int32_t s_scan[kWarps];
+    __shared__ int32_t s_inval;
+
+    griddep_wait();  // topk_idx and x come from earlier stream work
+    griddep_launch_dependents();
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const bool writer = blockIdx.x == 0;
+    for (int i = threadIdx.x; i < kWarps * wstride; i += kThreads) s_wc[i] = 0;
+    if (threadIdx.x == 0) s_inval = 0;
+    __syncthreads();
+
+    // each warp owns `sub` consecutive entries (a multiple of 32)
+    const int64_t sub = (a.n + kThreads - 1) / kThreads * 32;
+    const int64_t wbegin = (int64_t)warp * sub;
+    const int64_t wend = min(wbegin + sub, a.n);
+    int32_t *my_wc = s_wc + warp * wstride;
+
+    // per-warp counts
+    int invalid = 0;
+    for (int64_t c = wbegin; c < wend; c += 32) {
+        const int64_t i = c + lane;
+        const int k = entry_key(a, i, i < wend);
+        if (k == -1) ++invalid;
+        const unsigned peers = __match_any_sync(0xffffffffu, k);
+        if (k >= 0 && lane == __ffs(peers) - 1) my_wc[k] += __popc(peers);
+        __syncwarp();
+    }
+    for (int sh = 16; sh; sh >>= 1) invalid += __shfl_xor_sync(0xffffffffu, invalid, sh);
+    if (lane == 0 && invalid) atomicAdd(&s_inval, invalid);
+    __syncthreads();
+
+    // totals and bucket offsets (thread e owns expert e)
+    const int e = threadIdx.x;
+    int32_t tot = 0;
+    if (e < a.E)
+        for (int w = 0; w < kWarps; ++w) tot += s_wc[w * wstride + e];
+    int32_t total;
+    const int32_t offe = block_scan(tot, s_scan, total);
+    if (e < a.E) {
+        s_off[e] = offe;
+        if (writer) {
+            a.cnt[e] = tot;
+            a.off[e] = offe;
+        }
+    }
+    if (writer && threadIdx.x == 0) {
+        a.off[a.E] = total;
+        *a.n_invalid = s_inval;
+    }
+
+    // per expert, exclusive scan over the warps (lane l holds warp l)
+    for (int k = warp; k < a.E; k += kWarps) {
+        const int32_t c = s_wc[lane * wstride + k];
+        int32_t x = c;
+        for (int sh = 1; sh < 32; sh <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, x, sh);
+            if (lane >= sh) x += y;
+        }
+        s_wc[lane * wstride + k] = x - c;
+    }
+    __syncthreads();
+
+    // ranks
+    for (int64_t c = wbegin; c < wend; c += 32) {
+        const int64_t i = c + lane;
+        const int k = entry_key(a, i, i < wend);
+        const unsigned peers = __match_any_sync(0xffffffffu, k);
+        int32_t row = -1;
+        if (k >= 0) row = s_off[k] + my_wc[k] + __popc(peers & lanemask_lt());
+        __syncwarp();
+        if (k >= 0 && lane == __ffs(peers) - 1) my_wc[k] += __popc(peers);
+        __syncwarp();
+        if (i < wend) {
+            s_row[i] = row;
+            if (writer) {
+                a.map[i] = row;
+                if (row >= 0) a.src[row] = (int32_t)i;
+            }
+        }
+    }
+    __syncthreads();
+
+    // rows: unit = (token, segment); scale rows follow the row's segments
+    const int64_t per_tok = a.segs + a.ssegs;
+    const int64_t units = a.S * per_tok;
+    for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < units;
+         u += (int64_t)gridDim.x * kWarps) {
+        const int64_t s = u / per_tok;
+        const int64_t g = u - s * per_tok;
+        const bool is_row = g < a.segs;
+        const int64_t len = is_row ? a.row_bytes : a.scale_bytes;
+        const int64_t ob = (is_row ? g : g - a.segs) * kSeg + lane * 16;
+        if (ob >= len) continue;
+        const uint8_t *srow = (is_row ? a.x : a.xs) + s * len;
+        uint8_t *dst = is_row ? a.px : a.ps;
+        const uint4 v = ld_stream16(srow + ob);
+        for (int k = 0; k < a.K; ++k) {
+            const int32_t r = s_row[s * a.K + k];
+            if (r < 0) continue;
+            if (r < a.packed_rows)
+                st16(dst + (int64_t)r * len + ob, v);
+            else
+                atomicOr(&g_pd_error, kErrDispatchIndex);
+        }
+    }
+}
+
+} // namespace
+} // namespace moe
+
+using namespace moe;
+
+MOE_EXPORT int64_t moe_plan_dispatch_fused_max(void) { return kFusedMaxEntries; }
+
+MOE_EXPORT int moe_plan_dispatch(const int32_t *topk_idx, const void *x, int64_t S, int64_t H,
+                                 int dtype, int K, int E, const float *x_scales,
+                                 int64_t n_scales, int32_t *cnt, int64_t *off,
+                                 int32_t *packed_src, int64_t *tok_map, int32_t *n_invalid,
+                                 void *packed_x, int64_t packed_rows, float *packed_scales,
+                                 void *workspace, size_t workspace_bytes, moe_stream_t stream)
+{
+    const int es = elem_size(dtype);
+    if (es == 0 || S < 0 || H < 1 || K < 1 || K > 32 || E < 1 || E > 1024 || n_scales < 0 ||
+        n_scales > 256)
+        return MOE_EINVAL;
+    if (S * (int64_t)K >= ((int64_t)1 << 31)) return MOE_EINVAL;
+    if (!cnt || !off || !n_invalid) return MOE_EINVAL;
+    if (S > 0 && (!topk_idx || !x || !packed_src || !tok_map || !packed_x || packed_rows < 1))
+        return MOE_EINVAL;
+    if (S > 0 && n_scales > 0 && (!x_scales || !packed_scales)) return MOE_EINVAL;
+    const int64_t row_bytes = H * es;
+    if (S > 0) {
+        if (row_bytes % 16 || !aligned16(x) || !aligned16(packed_x)) return MOE_EALIGN;
+        if (n_scales > 0 &&
+            ((n_scales * 4) % 16 || !aligned16(x_scales) || !aligned16(packed_scales)))
+            return MOE_EALIGN;
+    }
+    const int64_t n = S * (int64_t)K;
+    if (n == 0 || n > kFusedMaxEntries) {
+        // throughput path: the two calls it fuses, back to back
+        if (int rc = moe_plan(topk_idx, S, K, E, cnt, off, packed_src, tok_map, n_invalid,
+                              workspace, workspace_bytes, stream))
+            return rc;
+        return moe_dispatch(x, S, H, dtype, K, tok_map, packed_x, packed_rows, x_scales,
+                            n_scales, packed_scales, stream);
+    }
+    PDArgs a = {};
+    a.idx = topk_idx;
+    a.S = S;
+    a.K = K;
+    a.E = E;
+    a.n = n;
+    a.x = static_cast<const uint8_t *>(x);
+    a.row_bytes = row_bytes;
+    a.xs = reinterpret_cast<const uint8_t *>(x_scales);
+    a.scale_bytes = n_scales > 0 ? n_scales * 4 : 0;
+    a.segs = (row_bytes + kSeg - 1) / kSeg;
+    a.ssegs = (a.scale_bytes + kSeg - 1) / kSeg;
+    a.cnt = cnt;
+    a.off = off;
+    a.src = packed_src;
+    a.map = tok_map;
+    a.n_invalid = n_invalid;
+    a.px = static_cast<uint8_t *>(packed_x);
+    a.ps = reinterpret_cast<uint8_t *>(packed_scales);
+    a.packed_rows = packed_rows;
+
+    const size_t smem = ((size_t)kWarps * (E | 1) + (size_t)E + (size_t)n) * sizeof(int32_t);
+    static KernelCache cache;
+    int per_sm = 0;
+    cudaError_t err = prepare_kernel(plan_dispatch_kernel, smem, kThreads, cache, &per_sm);
+    if (err != cudaSuccess || per_sm < 1) {
+        set_cuda_error(err != cudaSuccess ? err : cudaErrorInvalidConfiguration);
+        return MOE_ECUDA;
+    }
+    // one warp per (token, segment) unit, at most one CTA per SM
+    const int64_t units = S * (a.segs + a.ssegs);
+    int64_t blocks = (units + kWarps - 1) / kWarps;
+    if (blocks > sm_count()) blocks = sm_count();
+    if (blocks < 1) blocks = 1;
+    err = launch_pdl(plan_dispatch_kernel, dim3((unsigned)blocks), dim3(kThreads), smem,
+                     (cudaStream_t)stream, a);
+    if (err != cudaSuccess) {
+        set_cuda_error(err);
+        return MOE_ECUDA;
+    }
+    return check_launch();
+}
+
+namespace moe {
+// Reads and clears this file's device error bits.
+cudaError_t read_plan_dispatch_errors(uint32_t *flags)
+{
+    uint32_t zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(flags, g_pd_error, sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_pd_error, &zero, sizeof(uint32_t));
+    return e;
+}
+} // namespace moe

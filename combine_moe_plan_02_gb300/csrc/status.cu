@@ -50,13 +50,14 @@ MOE_EXPORT int moe_last_cuda_error(void) { return moe::t_last_cuda_error; }
 MOE_EXPORT int moe_device_errors(uint32_t *flags)
 {
     if (!flags) return MOE_EINVAL;
-    uint32_t a = 0, b = 0;
+    uint32_t a = 0, b = 0, c = 0;
     cudaError_t e = moe::read_dispatch_errors(&a);
     if (e == cudaSuccess) e = moe::read_combine_errors(&b);
+    if (e == cudaSuccess) e = moe::read_plan_dispatch_errors(&c);
     if (e != cudaSuccess) {
         moe::set_cuda_error(e);
         return MOE_ECUDA;
     }
-    *flags = a | b;
+    *flags = a | b | c;
     return MOE_OK;
 }

@@ -5,6 +5,7 @@
  * One GPU holds every expert.  A step is
  *   moe_plan      per-expert histogram, exclusive scan, stable slot map
  *   moe_dispatch  scatter each token row into its K per-expert buckets
+ *                 (moe_plan_dispatch: both in one launch for small batches)
  *   (expert computation by the caller: packed rows -> expert output rows y)
  *   moe_combine   gather each token's K output rows, weighted f32 sum
  *                 (moe_combine_fold: unweighted or weighted, with the sum
@@ -213,7 +214,7 @@ int moe_group_plan(const int32_t *topk_idx, const int64_t *tok_map, int64_t S, i
  *               do for moe_plan; E*capacity for moe_plan_capacity); a map
  *               entry at or past packed_rows is skipped and flagged (bit 1
  *               of moe_device_errors)
- * x_scales      f32 [S, n_scales] or NULL when n_scales == 0
+ * x_scales      f32 [S, n_scales] or NULL when n_scales == 0 (n_scales <= 256)
  * packed_scales f32 [packed_rows, n_scales] or NULL when n_scales == 0
  * Alignment: x, packed_x, x_scales, packed_scales 16-byte aligned; H*size
  * and n_scales*4 multiples of 16 (else MOE_EALIGN).
@@ -242,6 +243,29 @@ int moe_dispatch(const void *x, int64_t S, int64_t H, int dtype, int K,
 int moe_dispatch_quant_fp8(const void *x, int64_t S, int64_t H, int K,
                            const int64_t *tok_map, int block, void *packed_q,
                            float *packed_scales, int64_t packed_rows, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Plan and dispatch in one call  [ROCm/mori "EPv2 internode dispatch/combine
+ * over CCO/GDA": a throughput and a low-latency kernel family, chosen per
+ * call below a token-count crossover (512 tokens on that page); mori #448
+ * StdMoE note for the outputs].
+ *
+ * Computes exactly what moe_plan followed by moe_dispatch computes: the same
+ * cnt, off, packed_src, tok_map, n_invalid, packed_x and packed_scales, with
+ * the same arguments, layouts and rules as those two calls.  When
+ * 0 < S*K <= moe_plan_dispatch_fused_max() one kernel does both (every CTA
+ * ranks all entries in shared memory; the workspace is not used); otherwise
+ * the call enqueues moe_plan then moe_dispatch, and `workspace` follows
+ * moe_plan's rule (moe_plan_workspace_size).  All arguments are checked
+ * before anything is enqueued.
+ * ---------------------------------------------------------------------- */
+int64_t moe_plan_dispatch_fused_max(void);
+int moe_plan_dispatch(const int32_t *topk_idx, const void *x, int64_t S, int64_t H,
+                      int dtype, int K, int E, const float *x_scales, int64_t n_scales,
+                      int32_t *cnt, int64_t *off, int32_t *packed_src, int64_t *tok_map,
+                      int32_t *n_invalid, void *packed_x, int64_t packed_rows,
+                      float *packed_scales, void *workspace, size_t workspace_bytes,
+                      moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Dedup dispatch  [mori #448: ballot-dedup send, then convert_dispatch_output

@@ -127,6 +127,27 @@ def test_combine_fold_validation(L):
     assert c(y=MIS) == EALIGN
 
 
+def test_plan_dispatch_validation(L):
+    f = lambda **k: L.moe_plan_dispatch(k.get("idx", FAKE), k.get("x", FAKE), k.get("S", 16),
+                                        k.get("H", 64), k.get("dt", 0), k.get("K", 2),
+                                        k.get("E", 8), k.get("xs", None), k.get("ns", 0),
+                                        FAKE, FAKE, FAKE, FAKE, FAKE, k.get("px", FAKE),
+                                        k.get("rows", 32), k.get("ps", None), None, 0, None)
+    assert L.moe_plan_dispatch_fused_max() >= 256
+    assert f(dt=3) == EINVAL
+    assert f(E=0) == EINVAL and f(E=1025) == EINVAL
+    assert f(K=33) == EINVAL
+    assert f(rows=0) == EINVAL
+    assert f(ns=4) == EINVAL                  # scales without buffers
+    assert f(ns=257, xs=FAKE, ps=FAKE) == EINVAL
+    assert f(ns=3, xs=FAKE, ps=FAKE) == EALIGN
+    assert f(H=12) == EALIGN
+    assert f(x=MIS) == EALIGN
+    assert f(px=MIS) == EALIGN
+    # above the crossover the plan needs its workspace (none given here)
+    assert f(S=200000, K=8, E=64, rows=1600000) == EINVAL
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_abi, "_lib", None)
     monkeypatch.setattr(_abi, "LIB_PATH", str(tmp_path / "missing.so"))

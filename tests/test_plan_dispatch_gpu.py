@@ -1,0 +1,122 @@
+"""Plan and dispatch in one call (one fused launch for small batches, plan
+then dispatch above the crossover) against the CPU oracle's plan and
+dispatch: every output bit-exact, unmapped rows untouched, and the same bits
+as moe_plan followed by moe_dispatch."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+from tests import gpu_path  # noqa: E402
+
+np_ = gpu_path._np
+
+
+def _fused_max():
+    import combine_moe_plan_02_gb300 as moe
+    return int(moe.lib().moe_plan_dispatch_fused_max())
+
+
+def _run(wl, idx):
+    import combine_moe_plan_02_gb300 as moe
+    S, K, E, H = wl.S, wl.K, wl.E, wl.H
+    d = gpu_path.to_device(wl)
+    rows = max(S * K, 1)
+    plan = moe.Plan(gpu_path.poisoned((E,), torch.int32), gpu_path.poisoned((E + 1,), torch.int64),
+                    gpu_path.poisoned((rows,), torch.int32), gpu_path.poisoned((S, K), torch.int64),
+                    gpu_path.poisoned((1,), torch.int32))
+    px = gpu_path.poisoned((rows, H), d["x"].dtype)
+    ps = gpu_path.poisoned((rows, d["x_scales"].shape[1]), torch.float32) \
+        if "x_scales" in d else None
+    t_idx = torch.from_numpy(np.ascontiguousarray(idx)).cuda()
+    moe.moe_plan_dispatch(t_idx, d["x"], E, x_scales=d.get("x_scales"), out=plan, packed_x=px,
+                          packed_scales=ps)
+    torch.cuda.synchronize()
+    assert moe.moe_device_errors() == 0
+    return plan, px, ps, d, t_idx
+
+
+def _check(wl, idx=None):
+    idx = wl.topk_idx if idx is None else idx
+    plan, px, ps, d, t_idx = _run(wl, idx)
+    ref = oracle.plan(idx, wl.E)
+    assert np.array_equal(np_(plan.cnt), ref["cnt"])
+    assert np.array_equal(np_(plan.off), ref["off"])
+    assert np.array_equal(np_(plan.tok_map), ref["tok_map"])
+    assert int(plan.n_invalid.item()) == ref["n_invalid"]
+    V = int(ref["off"][-1])
+    assert np.array_equal(np_(plan.packed_src)[:V], ref["packed_src"][:V])
+    rows = max(wl.S * wl.K, 1)
+    want = oracle.dispatch(wl.x, ref["tok_map"], rows, fill=gpu_path.POISON)
+    assert np.array_equal(np_(px), want)       # rows past off[E] keep the poison
+    if ps is not None:
+        want_s = oracle.dispatch(wl.x_scales, ref["tok_map"], rows, fill=gpu_path.POISON)
+        assert np.array_equal(np_(ps).view(np.uint32), want_s.view(np.uint32))
+    # the same bits as the two separate calls
+    import combine_moe_plan_02_gb300 as moe
+    p2 = moe.moe_plan(t_idx, wl.E)
+    px2 = gpu_path.poisoned((rows, wl.H), d["x"].dtype)
+    ps2 = gpu_path.poisoned(tuple(ps.shape), torch.float32) if ps is not None else None
+    moe.moe_dispatch(d["x"], p2.tok_map, packed_x=px2, x_scales=d.get("x_scales"),
+                     packed_scales=ps2)
+    torch.cuda.synchronize()
+    assert torch.equal(p2.tok_map, plan.tok_map)
+    assert torch.equal(px2.view(torch.uint8), px.view(torch.uint8))
+    if ps is not None:
+        assert torch.equal(ps2.view(torch.int32), ps.view(torch.int32))
+
+
+@pytest.mark.parametrize("S", [1, 4, 8, 31, 32, 127, 128, 129, 512, 1024])
+def test_fp8_rows_and_scales(S):
+    """fp8 rows + 48 scales per row (H=6144, E=256, K=8): S*K = 1024 is the
+    last fused size, 1032 the first two-call size."""
+    _check(workloads.make("fp8small", seed=100 + S, S=S))
+
+
+@pytest.mark.parametrize("S,H,E,K", [(128, 7168, 64, 8), (3, 8, 1, 1), (32, 1032, 1024, 32),
+                                     (33, 256, 1024, 31), (1000, 64, 7, 1), (17, 2056, 257, 5)])
+def test_bf16_shapes(S, H, E, K):
+    _check(workloads.make("moonep", seed=S + E, S=S, H=H, E=E, K=K))
+
+
+def test_invalid_ids_and_repeats():
+    wl = workloads.make("fp8small", seed=7, S=100)
+    idx = wl.topk_idx.copy()
+    idx[0, :] = -1
+    idx[1, 3] = wl.E
+    idx[2, :] = 5           # one expert eight times
+    idx[50, 2:] = -7
+    _check(wl, idx)
+
+
+def test_crossover_covers_the_small_token_sizes():
+    assert _fused_max() >= 32 * 8
+
+
+def test_short_packed_buffer_is_flagged_not_written():
+    """packed_x with fewer rows than the plan fills: the rows past its end are
+    skipped and bit 1 of moe_device_errors is set."""
+    import combine_moe_plan_02_gb300 as moe
+    wl = workloads.make("fp8small", seed=9, S=16)
+    d = gpu_path.to_device(wl)
+    guard = gpu_path.poisoned((wl.S * wl.K + 64, wl.H), d["x"].dtype)
+    px = guard[:100]
+    moe.moe_plan_dispatch(d["topk_idx"], d["x"], wl.E, packed_x=px)
+    torch.cuda.synchronize()
+    assert moe.moe_device_errors() & 2
+    assert torch.all(guard[100:].view(torch.uint8) == gpu_path.POISON)
+    assert moe.moe_device_errors() == 0
+
+
+def test_empty_batch():
+    import combine_moe_plan_02_gb300 as moe
+    idx = torch.zeros(0, 8, dtype=torch.int32, device="cuda")
+    x = torch.zeros(0, 64, dtype=torch.bfloat16, device="cuda")
+    plan, _, _ = moe.moe_plan_dispatch(idx, x, 16)
+    torch.cuda.synchronize()
+    assert plan.cnt.sum().item() == 0 and plan.off.sum().item() == 0
