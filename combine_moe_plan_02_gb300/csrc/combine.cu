@@ -224,15 +224,28 @@ void (*select_kernel(int in_dt, int out_dt, int wm))(CombineArgs)
     return nullptr;
 }
 
+// Slices per row and steps per lane for a grid of `warp_slots` warps.
+void set_slices(CombineArgs &a, int64_t warp_slots)
+{
+    // slices: at most kMaxLaneSteps steps per lane per unit, slices of equal
+    // size; finer units even out the work of the persistent warps.  When the
+    // rows cannot fill every warp of the grid (small batches), rows are cut
+    // finer, down to one step per lane, so that more gathers are in flight
+    // at once; the summation order of an element never depends on this.
+    const int64_t lane_steps = (a.steps + 31) / 32;
+    int64_t slices = (lane_steps + kMaxLaneSteps - 1) / kMaxLaneSteps;
+    if (a.rows * slices < warp_slots) {
+        const int64_t want = (warp_slots + a.rows - 1) / a.rows;
+        slices = want < lane_steps ? want : lane_steps;
+    }
+    a.R = (int)((lane_steps + slices - 1) / slices);
+    a.slices = (int)((lane_steps + a.R - 1) / a.R);
+}
+
 int launch_combine(CombineArgs &a, int in_dt, int out_dt, int wm, cudaStream_t stream)
 {
     void (*fn)(CombineArgs) = select_kernel(in_dt, out_dt, wm);
     if (!fn) return MOE_EINVAL;
-    // slices: at most kMaxLaneSteps steps per lane per unit, slices of equal
-    // size; finer units even out the work of the persistent warps
-    const int64_t lane_steps = (a.steps + 31) / 32;
-    a.slices = (int)((lane_steps + kMaxLaneSteps - 1) / kMaxLaneSteps);
-    a.R = (int)((lane_steps + a.slices - 1) / a.slices);
     // one cache per (input, output, weight-mode) kernel
     static KernelCache caches[2][2][3];
     KernelCache &cache = caches[in_dt == MOE_F32][out_dt == MOE_F32][wm];
@@ -242,6 +255,7 @@ int launch_combine(CombineArgs &a, int in_dt, int out_dt, int wm, cudaStream_t s
         set_cuda_error(err != cudaSuccess ? err : cudaErrorInvalidConfiguration);
         return MOE_ECUDA;
     }
+    set_slices(a, (int64_t)sm_count() * per_sm * (kThreads / 32));
     const int64_t units = a.rows * a.slices;
     int64_t blocks = (units + kThreads / 32 - 1) / (kThreads / 32);
     const int64_t cap = (int64_t)sm_count() * per_sm;

@@ -203,12 +203,6 @@ __device__ __forceinline__ void bulk_s2g(void *gmem_dst, const void *smem_src, u
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
-// Bulk prefetch of [p, p + bytes) into L2 (no completion to wait for).
-__device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // Wait until at most N of this thread's bulk groups still read shared memory.
 template <int N>
 __device__ __forceinline__ void bulk_wait_read()

@@ -101,6 +101,22 @@ __global__ void __launch_bounds__(kThreads, 1) plan_dispatch_kernel(PDArgs a)
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const bool writer = blockIdx.x == 0;
+
+    // The rows do not depend on the plan: each warp loads the segment of its
+    // first (token, segment) unit now, so that the load overlaps the ranking.
+    const int64_t per_tok = a.segs + a.ssegs;
+    const int64_t units = a.S * per_tok;
+    const int64_t u0 = (int64_t)blockIdx.x * kWarps + warp;
+    uint4 v0 = make_uint4(0, 0, 0, 0);
+    {
+        const int64_t s = u0 / per_tok;
+        const int64_t g = u0 - s * per_tok;
+        const bool is_row = g < a.segs;
+        const int64_t len = is_row ? a.row_bytes : a.scale_bytes;
+        const int64_t ob = (is_row ? g : g - a.segs) * kSeg + lane * 16;
+        if (u0 < units && ob < len) v0 = ld_stream16((is_row ? a.x : a.xs) + s * len + ob);
+    }
+
     for (int i = threadIdx.x; i < kWarps * wstride; i += kThreads) s_wc[i] = 0;
     if (threadIdx.x == 0) s_inval = 0;
     __syncthreads();
@@ -177,10 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1) plan_dispatch_kernel(PDArgs a)
     __syncthreads();
 
     // rows: unit = (token, segment); scale rows follow the row's segments
-    const int64_t per_tok = a.segs + a.ssegs;
-    const int64_t units = a.S * per_tok;
-    for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < units;
-         u += (int64_t)gridDim.x * kWarps) {
+    for (int64_t u = u0; u < units; u += (int64_t)gridDim.x * kWarps) {
         const int64_t s = u / per_tok;
         const int64_t g = u - s * per_tok;
         const bool is_row = g < a.segs;
@@ -189,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) plan_dispatch_kernel(PDArgs a)
         if (ob >= len) continue;
         const uint8_t *srow = (is_row ? a.x : a.xs) + s * len;
         uint8_t *dst = is_row ? a.px : a.ps;
-        const uint4 v = ld_stream16(srow + ob);
+        const uint4 v = (u == u0) ? v0 : ld_stream16(srow + ob);
         for (int k = 0; k < a.K; ++k) {
             const int32_t r = s_row[s * a.K + k];
             if (r < 0) continue;

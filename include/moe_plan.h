@@ -83,12 +83,13 @@ int moe_last_cuda_error(void);
  * and set a bit instead.
  *   bit 0  dispatch: a bounded wait for a staged row ran out of time (the
  *          kernel stopped early; its output is incomplete)
- *   bit 1  dispatch: a map entry pointed outside the source or destination
- *          buffer (that row was not copied)
+ *   bit 1  dispatch (moe_dispatch*, moe_plan_dispatch): a map entry pointed
+ *          outside the source or destination buffer (that row was not
+ *          copied)
  *   bit 2  combine: a map entry pointed outside y, or a group row's source
  *          entry outside topk_w (that term was dropped)
- *   bit 3  combine: a bounded wait for staged rows ran out of time (the
- *          kernel stopped early; its output is incomplete)
+ *   bit 3  reserved for a combine that waits on staged rows; the combine
+ *          kernels of this version never wait and never set it
  * flags: HOST pointer to one uint32.  Synchronous: waits for the device. */
 int moe_device_errors(uint32_t *flags);
 

@@ -142,3 +142,21 @@ def test_fold_empty_batch():
     w = torch.zeros(0, 4, dtype=torch.float32, device="cuda")
     out, ow = moe.moe_combine_fold(y, w, tm)
     assert out.shape == (0, 64) and ow.shape == (0, 4)
+
+
+def test_combine_alternating_K_in_one_process():
+    """Calls whose shared-memory needs differ (K = 8, 1, 2, 8, 16, 2) in one
+    process: a smaller call must not lower the limit a larger one relies on."""
+    import combine_moe_plan_02_gb300 as moe
+    for K in (8, 1, 2, 8, 16, 2):
+        wl = workloads.make("moonep", seed=60 + K, S=40, H=264, K=K)
+        d = gpu_path.to_device(wl)
+        plan = moe.moe_plan(d["topk_idx"], wl.E)
+        packed = gpu_path.poisoned((wl.S * K, wl.H), torch.bfloat16)
+        moe.moe_dispatch(d["x"], plan.tok_map, packed_x=packed)
+        out = moe.moe_combine(packed, d["topk_w"], plan.tok_map)
+        torch.cuda.synchronize()
+        p = oracle.plan(wl.topk_idx, wl.E)
+        opk = oracle.dispatch(wl.x, p["tok_map"], wl.S * K)
+        ref = oracle.combine(opk, "bf16", wl.topk_w, p["tok_map"], wl.H, "bf16")
+        assert np.array_equal(np_(out), ref), K
