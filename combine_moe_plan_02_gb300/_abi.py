@@ -39,6 +39,7 @@ SIGNATURES = {
     "moe_plan_dispatch": (I32, [P, P, I64, I64, I32, I32, I32, P, I64, P, P, P, P, P, P, I64, P,
                                 P, SZ, P]),
     "moe_device_errors": (I32, [P]),
+    "moe_selftest_wait_timeout": (I32, [I64, P]),
 }
 
 _lib = None

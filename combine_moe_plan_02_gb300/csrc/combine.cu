@@ -30,7 +30,10 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 256;
+#ifndef MOE_COMBINE_THREADS
+#define MOE_COMBINE_THREADS 256
+#endif
+constexpr int kThreads = MOE_COMBINE_THREADS;
 constexpr int kKChunk = 8;   // map entries held in registers at a time
 #ifndef MOE_COMBINE_LANE_STEPS
 #define MOE_COMBINE_LANE_STEPS 4

@@ -181,6 +181,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return done != 0;
 }
 
+// Orders this thread's generic-proxy shared-memory accesses before later
+// async-proxy (bulk copy) accesses of the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Bulk (non-tensor) TMA copies ------------------------------------------------
 
 // global -> shared, completion signalled on `bar` as transaction bytes.

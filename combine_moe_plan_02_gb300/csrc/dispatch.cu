@@ -49,16 +49,35 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
-// Bounded wait for phase `parity` of `bar`; false after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity)
+// Bounded wait for phase `parity` of `bar`; false after `limit_ns`.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
+}
+
+// Self-test of the timeout path: one warp waits, through the same bounded
+// wait as the dispatch kernels, on an mbarrier phase that nothing completes
+// (no copy is issued and nothing arrives), records the dispatch timeout bit
+// when the limit expires, and returns.  Nothing else is touched.
+__global__ void __launch_bounds__(32) wait_selftest_kernel(uint64_t limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const bool landed = mbar_wait_bounded(&bar, 0, limit_ns);
+    if (!__all_sync(0xffffffffu, landed) && lane == 0)
+        atomicOr(&g_dispatch_error, kErrDispatchTimeout);
 }
 
 struct CopyArgs {
@@ -220,6 +239,9 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) dispatch_bulk_kernel(CopyAr
 // the first lane of each block stores the block's scale.
 // ---------------------------------------------------------------------------
 
+#ifndef MOE_QUANT_BULK
+#define MOE_QUANT_BULK 1
+#endif
 constexpr int kQThreads = 256;
 constexpr int kQMaxIters = 8;  // 256-element steps per lane group per unit
 
@@ -236,6 +258,53 @@ struct QuantArgs {
     uint8_t *q;               // [dst_rows, H] E4M3 codes
     float *scales;            // [dst_rows, H / block]
 };
+
+// Quantises the 8 bf16 values of one lane (one 16-byte word) for a block of
+// GL lanes: returns the 8 E4M3 codes (little-endian in two words) and the
+// block's scale.  All 32 lanes must call it together (block amax shuffle).
+template <int GL>
+__device__ __forceinline__ uint2 quant8(const uint4 v, bool active, float &scale_out)
+{
+    float f[8];
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        f[2 * q] = __uint_as_float(w4[q] << 16);
+        f[2 * q + 1] = __uint_as_float(w4[q] & 0xffff0000u);
+    }
+    float amax = 0.0f;
+    if (active) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(f[q]));
+    }
+#pragma unroll
+    for (int o = GL / 2; o > 0; o >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    // v / scale, correctly rounded, by Markstein's correction step
+    // (P. Markstein, IBM J. Res. Dev. 34(1), 1990): with y = RN(1/scale)
+    // and q = RN(v*y), the residual v - q*scale is exact under FMA and
+    // RN(q + residual*y) = RN(v/scale).  One reciprocal per block
+    // instead of a full division per element.  A zero residual means
+    // q0 is the exact quotient; returning it keeps the sign of -0.
+    const float y = __frcp_rn(scale);
+    auto quot = [&](float x) {
+        const float q0 = __fmul_rn(x, y);
+        const float r = __fmaf_rn(-q0, scale, x);
+        return r == 0.0f ? q0 : __fmaf_rn(r, y, q0);
+    };
+    uint32_t packed[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+            make_float2(quot(f[4 * q]), quot(f[4 * q + 1])), __NV_SATFINITE, __NV_E4M3);
+        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+            make_float2(quot(f[4 * q + 2]), quot(f[4 * q + 3])), __NV_SATFINITE, __NV_E4M3);
+        packed[q] = (uint32_t)lo | ((uint32_t)hi << 16);
+    }
+    scale_out = scale;
+    return make_uint2(packed[0], packed[1]);
+}
 
 template <int GL>  // lanes per block (block / 8)
 __global__ void __launch_bounds__(kQThreads, 2) dispatch_quant_kernel(QuantArgs a)
@@ -276,44 +345,9 @@ __global__ void __launch_bounds__(kQThreads, 2) dispatch_quant_kernel(QuantArgs 
             if (r >= a.R || it0 + r >= a.iters) break;  // uniform across the warp
             const int64_t e = ((int64_t)(it0 + r) * 32 + lane) * 8;
             const bool active = e < a.H;
-            float f[8];
-            const uint32_t w4[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                f[2 * q] = __uint_as_float(w4[q] << 16);
-                f[2 * q + 1] = __uint_as_float(w4[q] & 0xffff0000u);
-            }
-            float amax = 0.0f;
-            if (active) {
-#pragma unroll
-                for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(f[q]));
-            }
-#pragma unroll
-            for (int o = GL / 2; o > 0; o >>= 1)
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-            // v / scale, correctly rounded, by Markstein's correction step
-            // (P. Markstein, IBM J. Res. Dev. 34(1), 1990): with y = RN(1/scale)
-            // and q = RN(v*y), the residual v - q*scale is exact under FMA and
-            // RN(q + residual*y) = RN(v/scale).  One reciprocal per block
-            // instead of a full division per element.  A zero residual means
-            // q0 is the exact quotient; returning it keeps the sign of -0.
-            const float y = __frcp_rn(scale);
-            auto quot = [&](float v) {
-                const float q0 = __fmul_rn(v, y);
-                const float r = __fmaf_rn(-q0, scale, v);
-                return r == 0.0f ? q0 : __fmaf_rn(r, y, q0);
-            };
-            uint32_t packed[2];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-                    make_float2(quot(f[4 * q]), quot(f[4 * q + 1])), __NV_SATFINITE, __NV_E4M3);
-                const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-                    make_float2(quot(f[4 * q + 2]), quot(f[4 * q + 3])), __NV_SATFINITE,
-                    __NV_E4M3);
-                packed[q] = (uint32_t)lo | ((uint32_t)hi << 16);
-            }
+            float scale;
+            const uint2 codes = quant8<GL>(v[r], active, scale);
+            const uint32_t packed[2] = {codes.x, codes.y};
             const bool block_lead = (lane % GL) == 0;
             const int64_t b = e / a.block;
             for (int k = 0; k < K; ++k) {
@@ -326,6 +360,181 @@ __global__ void __launch_bounds__(kQThreads, 2) dispatch_quant_kernel(QuantArgs 
                 if (block_lead) a.scales[(int64_t)d * nb + b] = scale;
             }
         }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Quantising dispatch through shared memory.  Each token row is quantised
+// once: a warp pulls a 1024-element chunk of bf16 into a stage with a bulk
+// copy, its 32 lanes quantise it (256 elements per step, as above) into the
+// stage's code and scale areas, and lanes 0..K-1 push those to the K
+// destination rows with bulk copies -- the same ring as dispatch_bulk_kernel,
+// with the per-destination work reduced to two bulk stores.  Used when every
+// chunk's scale run is a whole number of 16-byte words (H a multiple of
+// 4 * block) and the scale buffer is 16-byte aligned.
+// ---------------------------------------------------------------------------
+
+#ifndef MOE_QB_CHUNK
+#define MOE_QB_CHUNK 1024
+#endif
+constexpr int kQBChunk = MOE_QB_CHUNK;                           // elements per stage
+constexpr int kQBStageBytes = kQBChunk * 2 + kQBChunk + kQBChunk / 16 * 4;  // in, codes, scales
+#ifndef MOE_QB_STAGES
+#define MOE_QB_STAGES 2
+#endif
+#ifndef MOE_QB_WARPS
+#define MOE_QB_WARPS 4
+#endif
+#ifndef MOE_QB_GROUP
+#define MOE_QB_GROUP 2
+#endif
+constexpr int kQBStages = MOE_QB_STAGES;
+constexpr int kQBWarps = MOE_QB_WARPS;
+constexpr int kQBGroup = MOE_QB_GROUP;   // 256-element steps quantised together
+// The quantisation is latency-bound (shuffle and division chains), so resident
+// warps matter more than ring depth: two 1024-element stages per warp leave
+// room for 32 warps per SM (55 us at the MoonEP shape), where four
+// 2048-element stages allowed 8 (75-90 us).
+
+struct QBulkArgs {
+    const uint8_t *x;         // bf16 [S, H]
+    int64_t S, H;
+    int K;
+    const int64_t *tok_map;   // [S, K]
+    int64_t dst_rows;
+    int block;
+    int64_t nb;               // scales per row, H / block
+    int n_chunks;             // chunks per row
+    uint8_t *q;               // [dst_rows, H]
+    uint8_t *sc;              // f32 [dst_rows, nb]
+};
+
+template <int GL>
+__global__ void __launch_bounds__(kQBWarps * 32) dispatch_quant_bulk_kernel(QBulkArgs a)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t bars[kQBWarps][kQBStages];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t *ring = smem + (size_t)warp * kQBStages * kQBStageBytes;
+    uint64_t *bar = bars[warp];
+
+    if (lane == 0) {
+        for (int st = 0; st < kQBStages; ++st) mbar_init(&bar[st], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    griddep_wait();  // the plan and earlier readers of the packed buffers are done
+    griddep_launch_dependents();
+
+    const int64_t n_items = a.S * a.n_chunks;
+    const int64_t gw = (int64_t)blockIdx.x * kQBWarps + warp;
+    const int64_t W = (int64_t)gridDim.x * kQBWarps;
+    if (gw >= n_items) return;
+    const int64_t n_mine = (n_items - gw + W - 1) / W;
+
+    int64_t dst_row[kQBStages];
+    int64_t issued = 0;
+
+    auto issue = [&](int64_t j, int st) {
+        issued = j + 1;
+        const int64_t it = gw + j * W;
+        const int64_t r = it / a.n_chunks;
+        const int c = (int)(it - r * a.n_chunks);
+        const int64_t e0 = (int64_t)c * kQBChunk;
+        const uint32_t elems = (uint32_t)min((int64_t)kQBChunk, a.H - e0);
+        if (lane == 0) {
+            uint8_t *stage = ring + (size_t)st * kQBStageBytes;
+            fence_proxy_async_smem();  // earlier reads of the stage come first
+            mbar_arrive_expect_tx(&bar[st], elems * 2);
+            bulk_g2s(stage, a.x + (r * a.H + e0) * 2, elems * 2, &bar[st]);
+        }
+        int64_t d = -1;
+        if (lane < a.K) d = __ldg(a.tok_map + r * a.K + lane);
+        if (d >= a.dst_rows || d < -1) {
+            atomicOr(&g_dispatch_error, kErrDispatchIndex);
+            d = -1;
+        }
+        dst_row[st] = d;
+    };
+
+#pragma unroll
+    for (int st = 0; st < kQBStages; ++st)
+        if (st < n_mine) issue(st, st);
+
+    bool ok = true;
+    int64_t consumed = 0;
+    for (int64_t j0 = 0; j0 < n_mine && ok; j0 += kQBStages) {
+#pragma unroll
+        for (int st = 0; st < kQBStages; ++st) {
+            const int64_t j = j0 + st;
+            if (j >= n_mine || !ok) break;
+            const bool landed = mbar_wait_bounded(&bar[st], (uint32_t)((j / kQBStages) & 1));
+            if (!__all_sync(0xffffffffu, landed)) {
+                ok = false;
+                break;
+            }
+            consumed = j + 1;
+            const int64_t it = gw + j * W;
+            const int64_t r = it / a.n_chunks;
+            const int c = (int)(it - r * a.n_chunks);
+            const int64_t e0 = (int64_t)c * kQBChunk;
+            const int elems = (int)min((int64_t)kQBChunk, a.H - e0);
+            uint8_t *in = ring + (size_t)st * kQBStageBytes;
+            uint8_t *codes = in + kQBChunk * 2;
+            float *scs = reinterpret_cast<float *>(codes + kQBChunk);
+            // kQBGroup independent 256-element steps at a time, so that their
+            // shuffle and division chains overlap; steps past a short last
+            // chunk run on zeros and store nothing
+#pragma unroll
+            for (int t0 = 0; t0 < kQBChunk / 256; t0 += kQBGroup) {
+                uint4 v[kQBGroup];
+                bool act[kQBGroup];
+#pragma unroll
+                for (int u = 0; u < kQBGroup; ++u) {
+                    const int e = (t0 + u) * 256 + lane * 8;
+                    act[u] = e < elems;
+                    v[u] = act[u] ? *reinterpret_cast<const uint4 *>(in + e * 2)
+                                  : make_uint4(0, 0, 0, 0);
+                }
+                float scale[kQBGroup];
+                uint2 cw[kQBGroup];
+#pragma unroll
+                for (int u = 0; u < kQBGroup; ++u) cw[u] = quant8<GL>(v[u], act[u], scale[u]);
+#pragma unroll
+                for (int u = 0; u < kQBGroup; ++u) {
+                    const int e = (t0 + u) * 256 + lane * 8;
+                    if (act[u]) {
+                        *reinterpret_cast<uint2 *>(codes + e) = cw[u];
+                        if ((lane % GL) == 0) scs[e / a.block] = scale[u];
+                    }
+                }
+            }
+            fence_proxy_async_smem();  // the codes and scales are visible to the bulk stores
+            __syncwarp();
+            const int64_t d = dst_row[st];
+            if (d >= 0) {
+                bulk_s2g(a.q + d * a.H + e0, codes, (uint32_t)elems);
+                bulk_s2g(a.sc + (d * a.nb + e0 / a.block) * 4, scs,
+                         (uint32_t)(elems / a.block) * 4);
+            }
+            bulk_commit();
+            const int prev = (st + kQBStages - 1) % kQBStages;
+            const int64_t jn = j - 1 + kQBStages;
+            if (j >= 1 && jn < n_mine) {
+                bulk_wait_read<1>();
+                __syncwarp();
+                issue(jn, prev);
+            }
+        }
+    }
+
+    bulk_wait_all();
+    if (!ok) {
+        if (lane == 0) atomicOr(&g_dispatch_error, kErrDispatchTimeout);
+        for (int64_t j = consumed; j < issued; ++j)
+            (void)mbar_wait_bounded(&bar[j % kQBStages], (uint32_t)((j / kQBStages) & 1));
     }
 }
 
@@ -446,6 +655,58 @@ MOE_EXPORT int moe_dispatch_dedup(const void *x, int64_t S, int64_t H, int dtype
     return launch_copy(a, (cudaStream_t)stream);
 }
 
+#if MOE_QUANT_BULK
+namespace moe {
+namespace {
+int launch_quant_bulk(const void *x, int64_t S, int64_t H, int K, const int64_t *tok_map,
+                      int block, void *packed_q, float *packed_scales, int64_t packed_rows,
+                      cudaStream_t stream)
+{
+    QBulkArgs a = {};
+    a.x = static_cast<const uint8_t *>(x);
+    a.S = S;
+    a.H = H;
+    a.K = K;
+    a.tok_map = tok_map;
+    a.dst_rows = packed_rows;
+    a.block = block;
+    a.nb = H / block;
+    a.n_chunks = (int)((H + kQBChunk - 1) / kQBChunk);
+    a.q = static_cast<uint8_t *>(packed_q);
+    a.sc = reinterpret_cast<uint8_t *>(packed_scales);
+    void (*fn)(QBulkArgs) = nullptr;
+    static KernelCache caches[5];
+    KernelCache *cache = nullptr;
+    switch (block) {
+    case 16: fn = dispatch_quant_bulk_kernel<2>; cache = &caches[0]; break;
+    case 32: fn = dispatch_quant_bulk_kernel<4>; cache = &caches[1]; break;
+    case 64: fn = dispatch_quant_bulk_kernel<8>; cache = &caches[2]; break;
+    case 128: fn = dispatch_quant_bulk_kernel<16>; cache = &caches[3]; break;
+    default: fn = dispatch_quant_bulk_kernel<32>; cache = &caches[4]; break;
+    }
+    const size_t smem = (size_t)kQBWarps * kQBStages * kQBStageBytes;
+    int per_sm = 0;
+    cudaError_t err = prepare_kernel(fn, smem, kQBWarps * 32, *cache, &per_sm);
+    if (err != cudaSuccess || per_sm < 1) {
+        set_cuda_error(err != cudaSuccess ? err : cudaErrorInvalidConfiguration);
+        return MOE_ECUDA;
+    }
+    const int64_t items = S * a.n_chunks;
+    int64_t blocks = (items + kQBWarps - 1) / kQBWarps;
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    err = launch_pdl(fn, dim3((unsigned)blocks), dim3(kQBWarps * 32), smem, stream, a);
+    if (err != cudaSuccess) {
+        set_cuda_error(err);
+        return MOE_ECUDA;
+    }
+    return check_launch();
+}
+} // namespace
+} // namespace moe
+#endif
+
 MOE_EXPORT int moe_dispatch_quant_fp8(const void *x, int64_t S, int64_t H, int K,
                                       const int64_t *tok_map, int block, void *packed_q,
                                       float *packed_scales, int64_t packed_rows,
@@ -459,6 +720,11 @@ MOE_EXPORT int moe_dispatch_quant_fp8(const void *x, int64_t S, int64_t H, int K
     if (!x || !tok_map || !packed_q || !packed_scales || packed_rows < 1) return MOE_EINVAL;
     if (!aligned16(x) || !aligned16(packed_q) || (reinterpret_cast<uintptr_t>(packed_scales) & 3u))
         return MOE_EALIGN;
+#if MOE_QUANT_BULK
+    if (H % (4 * block) == 0 && aligned16(packed_scales))
+        return launch_quant_bulk(x, S, H, K, tok_map, block, packed_q, packed_scales,
+                                 packed_rows, (cudaStream_t)stream);
+#endif
     QuantArgs a = {};
     a.x = static_cast<const uint8_t *>(x);
     a.S = S;
@@ -497,6 +763,13 @@ MOE_EXPORT int moe_dispatch_quant_fp8(const void *x, int64_t S, int64_t H, int K
         set_cuda_error(err);
         return MOE_ECUDA;
     }
+    return check_launch();
+}
+
+MOE_EXPORT int moe_selftest_wait_timeout(int64_t limit_ns, moe_stream_t stream)
+{
+    if (limit_ns < 1000 || limit_ns > 100000000) return MOE_EINVAL;  // 1 us .. 100 ms
+    wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((uint64_t)limit_ns);
     return check_launch();
 }
 

@@ -93,6 +93,15 @@ int moe_last_cuda_error(void);
  * flags: HOST pointer to one uint32.  Synchronous: waits for the device. */
 int moe_device_errors(uint32_t *flags);
 
+/* Self-test of the bounded-wait path (the pages have no counterpart; the
+ * dispatch kernels' mbarrier waits give up after 2 s and report instead of
+ * hanging).  Enqueues one warp that waits, through the same bounded wait, on
+ * an mbarrier phase that nothing will ever complete; after limit_ns
+ * nanoseconds (1e3 .. 1e8, else MOE_EINVAL) it sets bit 0 of
+ * moe_device_errors and returns.  No memory of the caller is touched and the
+ * CUDA context stays usable.  Asynchronous on `stream`. */
+int moe_selftest_wait_timeout(int64_t limit_ns, moe_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Plan  [mori #448: StdMoE note (packed_cnt, packed_src, i64 slot map with
  * -1) and routing-handle note (local_expert_count)].

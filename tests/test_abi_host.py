@@ -148,6 +148,11 @@ def test_plan_dispatch_validation(L):
     assert f(S=200000, K=8, E=64, rows=1600000) == EINVAL
 
 
+def test_selftest_wait_limits(L):
+    assert L.moe_selftest_wait_timeout(999, None) == EINVAL
+    assert L.moe_selftest_wait_timeout(100_000_001, None) == EINVAL
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_abi, "_lib", None)
     monkeypatch.setattr(_abi, "LIB_PATH", str(tmp_path / "missing.so"))

@@ -215,3 +215,23 @@ def test_no_device_errors_after_runs():
     import combine_moe_plan_02_gb300 as moe
     gpu_path.run(workloads.make("tiny", seed=0))
     assert moe.moe_device_errors() == 0
+
+
+def test_bounded_wait_times_out_and_reports():
+    """The dispatch kernels' mbarrier wait, run against a phase that nothing
+    completes, gives up after its limit, sets the timeout bit and leaves the
+    context usable (a plan runs right after and is checked)."""
+    import combine_moe_plan_02_gb300 as moe
+    L = moe.lib()
+    assert moe.moe_device_errors() == 0
+    assert L.moe_selftest_wait_timeout(2_000_000, None) == 0     # 2 ms
+    torch.cuda.synchronize()
+    assert moe.moe_device_errors() == 1
+    assert moe.moe_device_errors() == 0                          # read clears
+    assert L.moe_selftest_wait_timeout(10, None) == 1            # below 1 us: EINVAL
+    wl = workloads.make("tiny", seed=5)
+    d = gpu_path.to_device(wl)
+    plan = moe.moe_plan(d["topk_idx"], wl.E)
+    torch.cuda.synchronize()
+    ref = oracle.plan(wl.topk_idx, wl.E)
+    assert np.array_equal(plan.tok_map.cpu().numpy(), ref["tok_map"])

@@ -15,7 +15,7 @@ pytestmark = [pytest.mark.gpu,
 from tests import gpu_path  # noqa: E402
 
 
-def _run(x_bits: np.ndarray, idx: np.ndarray, E: int, block: int):
+def _run(x_bits: np.ndarray, idx: np.ndarray, E: int, block: int, sc_offset: int = 0):
     import combine_moe_plan_02_gb300 as moe
     S, H = x_bits.shape
     K = idx.shape[1]
@@ -23,15 +23,19 @@ def _run(x_bits: np.ndarray, idx: np.ndarray, E: int, block: int):
     x = torch.from_numpy(x_bits.view(np.int16)).to(dev).view(torch.bfloat16)
     plan = moe.moe_plan(torch.from_numpy(np.ascontiguousarray(idx)).to(dev), E)
     q = gpu_path.poisoned((max(S * K, 1), H), torch.uint8)
-    sc = gpu_path.poisoned((max(S * K, 1), H // block), torch.float32)
+    n_sc = max(S * K, 1) * (H // block)
+    # sc_offset floats into a larger buffer: a scale buffer that is only
+    # 4-byte aligned takes the register kernel instead of the bulk one
+    sc = gpu_path.poisoned((n_sc + sc_offset,), torch.float32)[sc_offset:].view(
+        max(S * K, 1), H // block)
     moe.moe_dispatch_quant_fp8(x, plan.tok_map, block=block, packed_q=q, packed_scales=sc)
     torch.cuda.synchronize()
     assert moe.moe_device_errors() == 0
     return q.cpu().numpy(), sc.cpu().numpy(), int(plan.off[-1].item())
 
 
-def _check(x_bits, idx, E, block):
-    q, sc, V = _run(x_bits, idx, E, block)
+def _check(x_bits, idx, E, block, sc_offset=0):
+    q, sc, V = _run(x_bits, idx, E, block, sc_offset)
     p = oracle.plan(idx, E)
     q0, sc0 = oracle.quant_fp8(x_bits, block)
     ref_q = oracle.dispatch(q0, p["tok_map"], V)
@@ -61,6 +65,19 @@ def test_small_token_shape(S):
 def test_block_sizes(block):
     wl = workloads.make("moonep", seed=block, S=257, H=768, E=16, K=3)
     _check(wl.x, wl.topk_idx, wl.E, block)
+
+
+@pytest.mark.timeout(600)
+@pytest.mark.parametrize("H", [4096, 2560, 1024])
+@pytest.mark.parametrize("block", [16, 128, 256])
+@pytest.mark.parametrize("sc_offset", [0, 1])
+def test_both_kernels(H, block, sc_offset):
+    """Rows that are whole multiples of 4 blocks with a 16-byte aligned scale
+    buffer go through shared memory and bulk stores (2048-element chunks and
+    a shorter last chunk); the others (H % (4*block) != 0, or a scale buffer
+    that is only 4-byte aligned) through the register kernel.  Same bits."""
+    wl = workloads.make("moonep", seed=H + block, S=131, H=H, E=32, K=6)
+    _check(wl.x, wl.topk_idx, wl.E, block, sc_offset)
 
 
 @pytest.mark.timeout(600)
