@@ -427,6 +427,89 @@ def _small_token_sweep(moe, torch, dev, stream, reps, res):
 # GPU leg
 # ---------------------------------------------------------------------------
 
+def _timed_calls(torch, stream, flush_l2, calls, n=10, warmup=3):
+    """Mean µs of each call in `calls` (name -> fn), L2 flushed before each
+    sequence, an event between the calls."""
+    for _ in range(warmup):
+        for fn in calls.values():
+            fn()
+    torch.cuda.synchronize()
+    ts = {k: [] for k in calls}
+    for i in range(n):
+        flush_l2(i & 0xFF)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+        ev[0].record(stream)
+        for j, fn in enumerate(calls.values()):
+            fn()
+            ev[j + 1].record(stream)
+        torch.cuda.synchronize()
+        for j, k in enumerate(calls):
+            ts[k].append(ev[j].elapsed_time(ev[j + 1]))
+    return {k: statistics.mean(v) * 1e3 for k, v in ts.items()}
+
+
+def other_workloads(torch, moe, dev, stream, flush_l2, peak):
+    """The skewed-routing and the dedup workloads through the same calls
+    (identity experts: the combine gathers the dispatched rows), per call."""
+    res = {}
+
+    def entry(us, nbytes):
+        gbs = nbytes / (us * 1e-6) / 1e9
+        return {"us": round(us, 2), "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                "algorithmic_bytes": int(nbytes)}
+
+    # Zipf(1.2) routing over 256 experts: buckets from ~S rows down to empty
+    wl = workloads.make("zipf", seed=0)
+    S, H, E, K = wl.S, wl.H, wl.E, wl.K
+    idx = torch.from_numpy(wl.topk_idx).to(dev)
+    w = torch.from_numpy(wl.topk_w).to(dev)
+    x = torch.from_numpy(wl.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    plan = moe.moe_plan(idx, E)
+    packed = torch.empty(S * K, H, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(S, H, dtype=torch.bfloat16, device=dev)
+    t = _timed_calls(torch, stream, flush_l2, {
+        "plan": lambda: moe.moe_plan(idx, E, out=plan, stream=stream),
+        "dispatch": lambda: moe.moe_dispatch(x, plan.tok_map, packed_x=packed, stream=stream),
+        "combine": lambda: moe.moe_combine(packed, w, plan.tok_map, out=out, stream=stream)})
+    V = int(plan.off[-1].item())
+    nby = algorithmic_bytes(S, H, E, K, V)
+    cnt = plan.cnt.cpu()
+    res["zipf"] = {"workload": f"zipf: S={S} H={H} E={E} K={K} bf16, Zipf(1.2) routing",
+                   "largest_bucket": int(cnt.max()), "empty_buckets": int((cnt == 0).sum()),
+                   **{k: entry(t[k], nby[k]) for k in t}}
+    del packed, out, x
+
+    # dedup: 8 virtual groups of 8 experts, f32 rows
+    wl = workloads.make("dedup", seed=0)
+    S, H, E, K, gs = wl.S, wl.H, wl.E, wl.K, wl.group_size
+    idx = torch.from_numpy(wl.topk_idx).to(dev)
+    w = torch.from_numpy(wl.topk_w).to(dev)
+    x = torch.from_numpy(wl.x).to(dev)
+    plan = moe.moe_plan(idx, E)
+    gp = moe.moe_group_plan(idx, plan.tok_map, E, gs)
+    grp_x = torch.empty(gp.max_rows, H, dtype=torch.float32, device=dev)
+    packed = torch.empty(S * K, H, dtype=torch.float32, device=dev)
+    gtok = torch.empty(gp.max_rows, H, dtype=torch.float32, device=dev)
+    out = torch.empty(S, H, dtype=torch.float32, device=dev)
+    t = _timed_calls(torch, stream, flush_l2, {
+        "plan": lambda: moe.moe_plan(idx, E, out=plan, stream=stream),
+        "group_plan": lambda: moe.moe_group_plan(idx, plan.tok_map, E, gs, out=gp, stream=stream),
+        "dispatch_dedup": lambda: moe.moe_dispatch_dedup(x, gp, grp_x=grp_x, packed_x=packed,
+                                                         stream=stream),
+        "combine_dedup": lambda: moe.moe_combine_dedup(packed, w, gp, gtok=gtok, out=out,
+                                                       stream=stream)})
+    V = int(plan.off[-1].item())
+    R = int(gp.goff[-1].item())
+    b = 4
+    nby = {"plan": algorithmic_bytes(S, H, E, K, V)["plan"],
+           "group_plan": S * K * (4 + 8) + S * K * 8 + R * (4 + 8 * K) + (E // gs) * 12,
+           "dispatch_dedup": S * H * b + 2 * R * H * b + V * H * b + R * (4 + 8 * K),
+           "combine_dedup": V * H * b + 2 * R * H * b + S * H * b + R * (4 + 8 * K) + S * K * 12}
+    res["dedup"] = {"workload": f"dedup: S={S} H={H} E={E} in {E // gs} groups, K={K} f32",
+                    "group_rows": R, **{k: entry(t[k], nby[k]) for k in t}}
+    return res
+
+
 def run_ours(args):
     import torch
 
@@ -643,6 +726,8 @@ def run_ours(args):
             "what": "bf16 rows -> E4M3 codes + f32 scale per 128 elements, K packed rows each"}
     if rank == 0 and not args.no_small_tokens:
         line["small_tokens"] = small_token_latency(dev)
+    if rank == 0 and not args.no_other_workloads:
+        line["other_workloads"] = other_workloads(torch, moe, dev, stream, flush_l2, peak)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
         line["cpu_baseline"]["host_cpus"] = os.cpu_count()
@@ -657,6 +742,8 @@ def run_ours(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the Zipf and dedup per-call timings")
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
