@@ -722,7 +722,7 @@ def run_ours(args):
         line["dispatch_quant_fp8"] = {
             "us": round(1e3 * tq, 2), "GB_per_s": round(qbytes / (tq / 1e3) / 1e9, 1),
             "frac_of_peak": round(qbytes / (tq / 1e3) / 1e9 / peak, 4),
-            "algorithmic_bytes": qbytes,
+            "algorithmic_bytes": qbytes, "traffic": kernel_traffic("dispatch_quant_fp8"),
             "what": "bf16 rows -> E4M3 codes + f32 scale per 128 elements, K packed rows each"}
     if rank == 0 and not args.no_small_tokens:
         line["small_tokens"] = small_token_latency(dev)
