@@ -62,13 +62,29 @@ struct CombineArgs {
     float *out_w;              // if set: [rows, K] weight fold (reads w[i, *])
 };
 
+// Element layout of a lane-step.  A warp-step covers 256 consecutive
+// elements (32 lanes x 8).  Contiguous layout: lane l owns elements
+// 8l..8l+7.  Quad layout (used when a row holds f32, input or output, and the
+// warp-step is whole): lane l owns 4l..4l+3 and 128+4l..128+4l+3, so that
+// each 16-byte f32 access of the warp covers 512 contiguous bytes and no
+// 32-byte sector is split between two instructions.  p is the lane-step
+// index (warp-step p >> 5, lane p & 31); f[0..3] and f[4..7] are the two
+// halves in element order.
 template <typename T> struct Io;
 
 template <> struct Io<__nv_bfloat16> {
     static constexpr int kVec = 1;  // 16-byte vectors per 8 elements
-    __device__ __forceinline__ static void load(uint4 (&v)[1], const uint8_t *row, int64_t p)
+    __device__ __forceinline__ static void load(uint4 (&v)[1], const uint8_t *row, int64_t p,
+                                                bool quad)
     {
-        v[0] = ld_stream16(row + p * 16);
+        if (!quad) {
+            v[0] = ld_stream16(row + p * 16);
+        } else {
+            const int64_t base = (p >> 5) * 512 + (p & 31) * 8;
+            const uint2 a = ld_stream8(row + base);
+            const uint2 b = ld_stream8(row + base + 256);
+            v[0] = make_uint4(a.x, a.y, b.x, b.y);
+        }
     }
     __device__ __forceinline__ static void widen(const uint4 (&v)[1], float (&f)[8])
     {
@@ -79,7 +95,8 @@ template <> struct Io<__nv_bfloat16> {
             f[2 * q + 1] = __uint_as_float(u[q] & 0xffff0000u);
         }
     }
-    __device__ __forceinline__ static void store(uint8_t *out_row, int64_t p, const float (&f)[8])
+    __device__ __forceinline__ static void store(uint8_t *out_row, int64_t p, const float (&f)[8],
+                                                 bool quad)
     {
         uint32_t u[4];
 #pragma unroll
@@ -87,16 +104,29 @@ template <> struct Io<__nv_bfloat16> {
             __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * q], f[2 * q + 1]);  // RNE
             u[q] = *reinterpret_cast<uint32_t *>(&b);
         }
-        st16(out_row + p * 16, make_uint4(u[0], u[1], u[2], u[3]));
+        if (!quad) {
+            st16(out_row + p * 16, make_uint4(u[0], u[1], u[2], u[3]));
+        } else {
+            const int64_t base = (p >> 5) * 512 + (p & 31) * 8;
+            st8(out_row + base, make_uint2(u[0], u[1]));
+            st8(out_row + base + 256, make_uint2(u[2], u[3]));
+        }
     }
 };
 
 template <> struct Io<float> {
     static constexpr int kVec = 2;
-    __device__ __forceinline__ static void load(uint4 (&v)[2], const uint8_t *row, int64_t p)
+    __device__ __forceinline__ static void load(uint4 (&v)[2], const uint8_t *row, int64_t p,
+                                                bool quad)
     {
-        v[0] = ld_stream16(row + p * 32);
-        v[1] = ld_stream16(row + p * 32 + 16);
+        if (!quad) {
+            v[0] = ld_stream16(row + p * 32);
+            v[1] = ld_stream16(row + p * 32 + 16);
+        } else {
+            const int64_t base = (p >> 5) * 1024 + (p & 31) * 16;
+            v[0] = ld_stream16(row + base);
+            v[1] = ld_stream16(row + base + 512);
+        }
     }
     __device__ __forceinline__ static void widen(const uint4 (&v)[2], float (&f)[8])
     {
@@ -105,12 +135,21 @@ template <> struct Io<float> {
         f[4] = __uint_as_float(v[1].x); f[5] = __uint_as_float(v[1].y);
         f[6] = __uint_as_float(v[1].z); f[7] = __uint_as_float(v[1].w);
     }
-    __device__ __forceinline__ static void store(uint8_t *out_row, int64_t p, const float (&f)[8])
+    __device__ __forceinline__ static void store(uint8_t *out_row, int64_t p, const float (&f)[8],
+                                                 bool quad)
     {
-        st16(out_row + p * 32, make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
-                                          __float_as_uint(f[2]), __float_as_uint(f[3])));
-        st16(out_row + p * 32 + 16, make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]),
-                                               __float_as_uint(f[6]), __float_as_uint(f[7])));
+        const uint4 a = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                                   __float_as_uint(f[2]), __float_as_uint(f[3]));
+        const uint4 b = make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]),
+                                   __float_as_uint(f[6]), __float_as_uint(f[7]));
+        if (!quad) {
+            st16(out_row + p * 32, a);
+            st16(out_row + p * 32 + 16, b);
+        } else {
+            const int64_t base = (p >> 5) * 1024 + (p & 31) * 16;
+            st16(out_row + base, a);
+            st16(out_row + base + 512, b);
+        }
     }
 };
 
@@ -123,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, MOE_COMBINE_MIN_BLOCKS) combine_kern
     griddep_wait();  // y, map, weights come from earlier stream work
     griddep_launch_dependents();
 
+    constexpr bool kQuad = sizeof(Tin) == 4 || sizeof(Tout) == 4;
     const int lane = threadIdx.x & 31;
     const int64_t gw = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
     const int64_t W = ((int64_t)gridDim.x * kThreads) >> 5;
@@ -173,6 +213,9 @@ __global__ void __launch_bounds__(kThreads, MOE_COMBINE_MIN_BLOCKS) combine_kern
         for (int r = 0; r < a.R; ++r) {
             const int64_t p = pbase + (int64_t)r * 32 + lane;
             const bool active = p < a.steps;
+            // quad layout when f32 is involved and the warp-step is whole
+            // (the same for every lane: pbase is a multiple of 32)
+            const bool quad = kQuad && (((p >> 5) + 1) << 5) <= a.steps;
             float acc[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
@@ -185,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, MOE_COMBINE_MIN_BLOCKS) combine_kern
                 for (int kk = 0; kk < kKChunk; ++kk) {
                     rk[kk] = __shfl_sync(0xffffffffu, my_row, (k0 + kk) & 31);
                     if (active && k0 + kk < K && rk[kk] >= 0)
-                        Io<Tin>::load(v[kk], a.y + (int64_t)rk[kk] * in_row_bytes, p);
+                        Io<Tin>::load(v[kk], a.y + (int64_t)rk[kk] * in_row_bytes, p, quad);
                 }
 #pragma unroll
                 for (int kk = 0; kk < kKChunk; ++kk) {
@@ -203,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, MOE_COMBINE_MIN_BLOCKS) combine_kern
                     }
                 }
             }
-            if (active) Io<Tout>::store(out_row, p, acc);
+            if (active) Io<Tout>::store(out_row, p, acc, quad);
         }
     }
 }

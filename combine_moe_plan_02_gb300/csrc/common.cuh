@@ -230,6 +230,18 @@ __device__ __forceinline__ uint4 ld_stream16(const void *p)
     return v;
 }
 
+__device__ __forceinline__ uint2 ld_stream8(const void *p)
+{
+    uint2 v;
+    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st8(void *p, uint2 v)
+{
+    asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
 __device__ __forceinline__ void st16(void *p, uint4 v)
 {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
