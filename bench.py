@@ -503,8 +503,11 @@ def other_workloads(torch, moe, dev, stream, flush_l2, peak):
     b = 4
     nby = {"plan": algorithmic_bytes(S, H, E, K, V)["plan"],
            "group_plan": S * K * (4 + 8) + S * K * 8 + R * (4 + 8 * K) + (E // gs) * 12,
-           "dispatch_dedup": S * H * b + 2 * R * H * b + V * H * b + R * (4 + 8 * K),
-           "combine_dedup": V * H * b + 2 * R * H * b + S * H * b + R * (4 + 8 * K) + S * K * 12}
+           # x read once, group rows and packed rows written (one pass: the
+           # group rows are not read back)
+           "dispatch_dedup": S * H * b + R * H * b + V * H * b + R * (4 + 8 * K),
+           # expert rows read, group-row sums and token sums written (one pass)
+           "combine_dedup": V * H * b + R * H * b + S * H * b + R * 8 * K + S * K * 16}
     res["dedup"] = {"workload": f"dedup: S={S} H={H} E={E} in {E // gs} groups, K={K} f32",
                     "group_rows": R, **{k: entry(t[k], nby[k]) for k in t}}
     return res

@@ -251,6 +251,138 @@ __global__ void __launch_bounds__(kThreads, MOE_COMBINE_MIN_BLOCKS) combine_kern
     }
 }
 
+// ---------------------------------------------------------------------------
+// Dedup combine in one pass (K <= kKChunk).  The work unit is (token s,
+// slice).  Lane k holds the token's group-row entry gtok_map[s,k] (set for the
+// first entry of each group: the representatives, in increasing k) and, after
+// one load per representative, the y row of its own entry and the index of
+// the representative whose group it is in.  Per step all of the token's
+// gathers are issued first; then, representative by representative in k
+// order, the group row's weighted sum is formed in increasing k (exactly the
+// first stage), stored to gtok, and added to the token's sum (exactly the
+// second stage), so gtok is written but never read back.  The weights come
+// from the token's own row, which is grp_src[r] / K for every group row r of
+// the token in a plan from moe_group_plan.
+// ---------------------------------------------------------------------------
+
+struct DedupArgs {
+    const uint8_t *y;          // expert outputs [y_rows, H]
+    int64_t y_rows;
+    const float *w;            // [S, K]
+    const int64_t *gtok_map;   // [S, K]
+    const int64_t *grp_tok_map;  // [max_rows, K]
+    int64_t max_rows;
+    int64_t S;
+    int K;
+    int64_t steps;             // H / 8
+    int R, slices;
+    float *gtok;               // [max_rows, H] f32
+    uint8_t *out;              // [S, H]
+};
+
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(kThreads, MOE_COMBINE_MIN_BLOCKS)
+combine_dedup_kernel(DedupArgs a)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+
+    constexpr bool kQuad = sizeof(Tin) == 4 || sizeof(Tout) == 4;
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+    const int64_t W = ((int64_t)gridDim.x * kThreads) >> 5;
+    const int64_t units = a.S * a.slices;
+    const int K = a.K;
+    constexpr int kInBytes = (int)sizeof(Tin) * 8;
+    constexpr int kOutBytes = (int)sizeof(Tout) * 8;
+    const int64_t in_row_bytes = a.steps * kInBytes;
+    const int64_t out_row_bytes = a.steps * kOutBytes;
+    const int64_t g_row_bytes = a.steps * 32;  // gtok rows are f32
+
+    for (int64_t u = gw; u < units; u += W) {
+        const int64_t s = u / a.slices;
+        const int sl = (int)(u - s * a.slices);
+        // lane k: the token's group-row entry (representatives only)
+        int64_t gk = -1;
+        if (lane < K) {
+            gk = __ldg(a.gtok_map + s * K + lane);
+            if (gk < -1 || gk >= a.max_rows) {
+                atomicOr(&g_combine_error, kErrCombineIndex);
+                gk = -1;
+            }
+        }
+        const unsigned reps = __ballot_sync(0xffffffffu, gk >= 0);
+        // lane k: its y row and the rank of its representative (k order)
+        int32_t my_row = -1;
+        int my_rep = -1;
+        {
+            unsigned m = reps;
+            for (int j = 0; m; ++j, m &= m - 1) {
+                const int q = __ffs(m) - 1;
+                const int64_t rq = __shfl_sync(0xffffffffu, gk, q);
+                if (lane < K) {
+                    const int64_t e = __ldg(a.grp_tok_map + rq * K + lane);
+                    if (e >= 0 && e < a.y_rows) {
+                        my_row = (int32_t)e;
+                        my_rep = j;
+                    } else if (e != -1) {
+                        atomicOr(&g_combine_error, kErrCombineIndex);
+                    }
+                }
+            }
+        }
+        const float my_w = (lane < K && my_row >= 0) ? __ldg(a.w + s * K + lane) : 0.0f;
+        int32_t rk[kKChunk], jk[kKChunk];
+        float wk[kKChunk];
+#pragma unroll
+        for (int kk = 0; kk < kKChunk; ++kk) {
+            rk[kk] = __shfl_sync(0xffffffffu, my_row, kk);
+            jk[kk] = __shfl_sync(0xffffffffu, my_rep, kk);
+            wk[kk] = __shfl_sync(0xffffffffu, my_w, kk);
+        }
+        const int n_reps = __popc(reps);
+        const int64_t pbase = (int64_t)sl * 32 * a.R;
+        uint8_t *out_row = a.out + s * out_row_bytes;
+
+        for (int r = 0; r < a.R; ++r) {
+            const int64_t p = pbase + (int64_t)r * 32 + lane;
+            const bool active = p < a.steps;
+            const bool quad = kQuad && (((p >> 5) + 1) << 5) <= a.steps;
+            uint4 v[kKChunk][Io<Tin>::kVec];
+#pragma unroll
+            for (int kk = 0; kk < kKChunk; ++kk)
+                if (active && kk < K && rk[kk] >= 0)
+                    Io<Tin>::load(v[kk], a.y + (int64_t)rk[kk] * in_row_bytes, p, quad);
+            float tot[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) tot[q] = 0.0f;
+            unsigned m = reps;
+            for (int j = 0; j < n_reps; ++j, m &= m - 1) {
+                const int64_t rq = __shfl_sync(0xffffffffu, gk, __ffs(m) - 1);
+                float acc[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+#pragma unroll
+                for (int kk = 0; kk < kKChunk; ++kk) {
+                    if (active && kk < K && rk[kk] >= 0 && jk[kk] == j) {
+                        float f[8];
+                        Io<Tin>::widen(v[kk], f);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], __fmul_rn(wk[kk], f[q]));
+                    }
+                }
+                if (active) {
+                    Io<float>::store(reinterpret_cast<uint8_t *>(a.gtok) + rq * g_row_bytes, p, acc,
+                                     quad);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) tot[q] = __fadd_rn(tot[q], acc[q]);
+                }
+            }
+            if (active) Io<Tout>::store(out_row, p, tot, quad);
+        }
+    }
+}
+
 template <typename Tin, typename Tout>
 void (*pick_kernel(int wm))(CombineArgs)
 {
@@ -317,6 +449,41 @@ int launch_combine(CombineArgs &a, int in_dt, int out_dt, int wm, cudaStream_t s
 
 bool combine_dtype_ok(int dt) { return dt == MOE_BF16 || dt == MOE_F32; }
 
+int launch_dedup(DedupArgs &d, int in_dt, int out_dt, cudaStream_t stream)
+{
+    void (*fn)(DedupArgs) = nullptr;
+    if (in_dt == MOE_BF16 && out_dt == MOE_BF16) fn = combine_dedup_kernel<__nv_bfloat16, __nv_bfloat16>;
+    if (in_dt == MOE_BF16 && out_dt == MOE_F32) fn = combine_dedup_kernel<__nv_bfloat16, float>;
+    if (in_dt == MOE_F32 && out_dt == MOE_BF16) fn = combine_dedup_kernel<float, __nv_bfloat16>;
+    if (in_dt == MOE_F32 && out_dt == MOE_F32) fn = combine_dedup_kernel<float, float>;
+    if (!fn) return MOE_EINVAL;
+    static KernelCache caches[2][2];
+    KernelCache &cache = caches[in_dt == MOE_F32][out_dt == MOE_F32];
+    int per_sm = 0;
+    cudaError_t err = prepare_kernel(fn, 0, kThreads, cache, &per_sm);
+    if (err != cudaSuccess || per_sm < 1) {
+        set_cuda_error(err != cudaSuccess ? err : cudaErrorInvalidConfiguration);
+        return MOE_ECUDA;
+    }
+    CombineArgs geo = {};
+    geo.rows = d.S;
+    geo.steps = d.steps;
+    set_slices(geo, (int64_t)sm_count() * per_sm * (kThreads / 32));
+    d.R = geo.R;
+    d.slices = geo.slices;
+    const int64_t units = d.S * d.slices;
+    int64_t blocks = (units + kThreads / 32 - 1) / (kThreads / 32);
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    err = launch_pdl(fn, dim3((unsigned)blocks), dim3(kThreads), 0, stream, d);
+    if (err != cudaSuccess) {
+        set_cuda_error(err);
+        return MOE_ECUDA;
+    }
+    return check_launch();
+}
+
 } // namespace
 } // namespace moe
 
@@ -358,6 +525,22 @@ MOE_EXPORT int moe_combine_dedup(const void *y, int in_dtype, const float *topk_
         return MOE_EINVAL;
     if (max_rows < S * (int64_t)(K < G ? K : G)) return MOE_EINVAL;
     if (H % 8 || !aligned16(y) || !aligned16(out) || !aligned16(gtok)) return MOE_EALIGN;
+    if (K <= kKChunk) {
+        DedupArgs d = {};
+        d.y = static_cast<const uint8_t *>(y);
+        d.y_rows = S * (int64_t)K;
+        d.w = topk_w;
+        d.gtok_map = gtok_map;
+        d.grp_tok_map = grp_tok_map;
+        d.max_rows = max_rows;
+        d.S = S;
+        d.K = K;
+        d.steps = H / 8;
+        d.gtok = gtok;
+        d.out = static_cast<uint8_t *>(out);
+        return launch_dedup(d, in_dtype, out_dtype, (cudaStream_t)stream);
+    }
+    // K > kKChunk: two passes
     // stage 1: per group row, weighted sum of its experts' outputs (f32)
     CombineArgs a = {};
     a.y = static_cast<const uint8_t *>(y);

@@ -98,6 +98,8 @@ struct CopyArgs {
     uint8_t *sdst;
     int scale_bytes;           // multiple of 16 (0 = none)
     int stage_bytes;           // chunk + scale area, multiple of 128
+    uint8_t *dst2;             // with dst_map and K < 32: lane K also stores item row r here
+    int64_t dst2_rows;         // rows of dst2 (bounds check)
 };
 
 __global__ void __launch_bounds__(kWarpsPerCta * 32) dispatch_bulk_kernel(CopyArgs a)
@@ -155,13 +157,16 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) dispatch_bulk_kernel(CopyAr
             }
         }
         int64_t d = -1;
+        const bool second = a.dst2 != nullptr && lane == a.K;  // the item's own copy
         if (a.dst_map) {
             if (lane < a.K) d = __ldg(a.dst_map + r * a.K + lane);
+            else if (second) d = r;
         } else if (lane == 0) {
             d = r;
         }
-        if (d >= a.dst_rows || d < -1 || (d >= 0 && !src_ok)) {
-            if (d >= a.dst_rows || d < -1) atomicOr(&g_dispatch_error, kErrDispatchIndex);
+        const int64_t lim = second ? a.dst2_rows : a.dst_rows;
+        if (d >= lim || d < -1 || (d >= 0 && !src_ok)) {
+            if (d >= lim || d < -1) atomicOr(&g_dispatch_error, kErrDispatchIndex);
             d = -1;
         }
         dst_row[st] = d;
@@ -195,9 +200,13 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) dispatch_bulk_kernel(CopyAr
             const uint8_t *stage = ring + (size_t)st * a.stage_bytes;
             const int64_t d = dst_row[st];
             if (d >= 0) {
-                bulk_s2g(a.dst + d * a.row_bytes + off, stage, bytes);
-                if (a.scale_bytes > 0 && c == 0)
-                    bulk_s2g(a.sdst + d * a.scale_bytes, stage + a.chunk, a.scale_bytes);
+                if (a.dst2 != nullptr && lane == a.K) {
+                    bulk_s2g(a.dst2 + d * a.row_bytes + off, stage, bytes);
+                } else {
+                    bulk_s2g(a.dst + d * a.row_bytes + off, stage, bytes);
+                    if (a.scale_bytes > 0 && c == 0)
+                        bulk_s2g(a.sdst + d * a.scale_bytes, stage + a.chunk, a.scale_bytes);
+                }
             }
             bulk_commit();
             // refill the stage of item j-1 with item j-1+kStages once the
@@ -634,6 +643,22 @@ MOE_EXPORT int moe_dispatch_dedup(const void *x, int64_t S, int64_t H, int dtype
     a.chunk = pick_chunk(row_bytes, &a.n_chunks);
     a.rows = max_rows;
     a.rows_dev = goff + G;
+    if (K < 32) {
+        // one pass: each chunk of x[grp_src[r] / K] is staged once and stored
+        // to the group row r and to the packed rows of its experts
+        a.src = static_cast<const uint8_t *>(x);
+        a.src_map = grp_src;
+        a.src_div = K;
+        a.src_rows = S;
+        a.dst = static_cast<uint8_t *>(packed_x);
+        a.dst_map = grp_tok_map;
+        a.K = K;
+        a.dst_rows = S * (int64_t)K;
+        a.dst2 = static_cast<uint8_t *>(grp_x);
+        a.dst2_rows = max_rows;
+        return launch_copy(a, (cudaStream_t)stream);
+    }
+    // K = 32 leaves no lane for the group row: two passes
     // stage 1: one copy of the token per group row
     a.src = static_cast<const uint8_t *>(x);
     a.dst = static_cast<uint8_t *>(grp_x);

@@ -122,7 +122,9 @@ struct DirectKey {
         int e = __ldg(idx + i);
         return (e >= 0 && e < E) ? e : -1;
     }
-    __device__ __forceinline__ void emit(int64_t, int64_t, int, const RankOut &) const {}
+    __device__ __forceinline__ void emit_chunk(int64_t, bool, int64_t, int, const RankOut &) const
+    {
+    }
 
     static constexpr bool kMergesWarpCounts = true;
 
@@ -227,9 +229,29 @@ struct GroupKey {
             if (group(j) == g) return -1;
         return g;
     }
-    // A representative lists its token's experts that fall in its group.
-    __device__ __forceinline__ void emit(int64_t i, int64_t row, int g, const RankOut &o) const
+    // Each representative row lists its token's experts that fall in its
+    // group (the direct plan's row, else -1).  Called by all lanes of a chunk
+    // together; `row` >= 0 marks a representative.  When tokens sit whole in
+    // a chunk (32 % K == 0) the lanes of a token fill the rows together:
+    // lane j writes column j of every representative row of its token, from
+    // its own entry.  Otherwise each representative walks its token.
+    __device__ __forceinline__ void emit_chunk(int64_t i, bool in_range, int64_t row, int g,
+                                               const RankOut &o) const
     {
+        if ((32 % K) == 0) {
+            const int lane = threadIdx.x & 31;
+            const int base = lane - lane % K;
+            const int gj = in_range ? group(i) : -1;
+            const int64_t tm = in_range ? o.tok_map[i] : -1;
+            for (int kk = 0; kk < K; ++kk) {
+                const int64_t rq = __shfl_sync(0xffffffffu, row, base + kk);
+                const int gq = __shfl_sync(0xffffffffu, g, base + kk);
+                if (rq >= 0 && in_range)
+                    o.grp_tok_map[rq * K + (lane - base)] = (gj == gq) ? tm : -1;
+            }
+            return;
+        }
+        if (row < 0 || !in_range) return;
         const int64_t s0 = i - i % K;
         for (int kk = 0; kk < K; ++kk)
             o.grp_tok_map[row * K + kk] = (group(s0 + kk) == g) ? o.tok_map[s0 + kk] : -1;
@@ -245,6 +267,31 @@ struct GroupKey {
                                              int, int32_t *s_tot, int32_t *s_bef, int32_t *) const
     {
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        const int G = E / gs;
+        if (G <= 32) {
+            // lane g tallies group g in registers (one ballot per group and
+            // chunk), then adds once: no contended shared-memory atomics
+            int bef = 0, aft = 0;
+            for (int64_t c = (int64_t)warp * 32; c < n; c += (int64_t)kWarps * 32) {
+                const int64_t i = c + lane;
+                const int k = chunk_key(i, i < n);
+                const bool before = c < tile_begin;
+                for (int gg = 0; gg < G; ++gg) {
+                    const int cnt = __popc(__ballot_sync(0xffffffffu, k == gg));
+                    if (lane == gg) {
+                        if (before)
+                            bef += cnt;
+                        else
+                            aft += cnt;
+                    }
+                }
+            }
+            if (lane < G) {
+                if (bef) atomicAdd(&s_bef[lane], bef);
+                if (aft) atomicAdd(&s_tot[lane], aft);
+            }
+            return 0;
+        }
         for (int64_t c = (int64_t)warp * 32; c < n; c += (int64_t)kWarps * 32) {
             const int64_t i = c + lane;
             const int k = chunk_key(i, i < n);
@@ -468,11 +515,9 @@ __global__ void __launch_bounds__(kThreads, 1) plan_rank_kernel(Key key, int nke
         __syncwarp();
         if (i < wend) {
             o.map[i] = row;
-            if (row >= 0) {
-                o.src[row] = (int32_t)i;
-                key.emit(i, row, k, o);
-            }
+            if (row >= 0) o.src[row] = (int32_t)i;
         }
+        key.emit_chunk(i, i < wend, row, k, o);
     }
 }
 

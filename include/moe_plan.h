@@ -279,9 +279,12 @@ int moe_plan_dispatch(const int32_t *topk_idx, const void *x, int64_t S, int64_t
 
 /* ------------------------------------------------------------------------
  * Dedup dispatch  [mori #448: ballot-dedup send, then convert_dispatch_output
- * per (received token, k)].  Two stages on `stream`:
+ * per (received token, k)].  Writes, on `stream`:
  *   grp_x[r, :]                = x[grp_src[r] / K, :]          r < R = goff[G]
  *   packed_x[grp_tok_map[r,k]] = grp_x[r, :]      for grp_tok_map[r,k] >= 0
+ * For K < 32 both come from one pass (each chunk of the source row is staged
+ * once and stored to the group row and to its experts' packed rows); K = 32
+ * takes two passes, the second reading grp_x.
  * max_rows: rows allocated for grp_x (and grp_src/grp_tok_map); must be at
  * least S * min(K, G), which bounds R.  Alignment as moe_dispatch.
  * ---------------------------------------------------------------------- */
@@ -318,8 +321,12 @@ int moe_combine(const void *y, int64_t y_rows, int in_dtype, const float *topk_w
  *                topk_w[s,k] * y[grp_tok_map[r,k], j]     (f32, s = grp_src[r]/K)
  *   out[s, j]  = round_out( sum over k with gtok_map[s,k] >= 0 of
  *                           gtok[gtok_map[s,k], j] )      (f32, unweighted)
- * gtok: f32 [max_rows, H] device scratch written by the first stage (it is
- * also the per-group result and may be read afterwards).
+ * gtok: f32 [max_rows, H], written with the group-row sums (the per-group
+ * result; it may be read afterwards).  For K <= 8 one pass computes both
+ * sums from the same gathers, in the order above, and never reads gtok back
+ * (the weights of a group row are then read from the token's own row, which
+ * is grp_src[r] / K in a plan from moe_group_plan); larger K takes two
+ * passes.
  * max_rows >= S * min(K, G).  Alignment as moe_combine.
  * ---------------------------------------------------------------------- */
 int moe_combine_dedup(const void *y, int in_dtype, const float *topk_w,

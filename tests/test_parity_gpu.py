@@ -158,7 +158,7 @@ def test_repeated_expert_within_token():
 
 
 @pytest.mark.timeout(600)
-@pytest.mark.parametrize("gs,K", [(1, 8), (2, 3), (16, 8), (64, 8), (4, 6)])
+@pytest.mark.parametrize("gs,K", [(1, 8), (2, 3), (16, 8), (64, 8), (4, 6), (2, 32), (8, 31)])
 def test_dedup_group_sizes(gs, K):
     wl = workloads.make("dedup", seed=gs * 10 + K, S=700, H=64, K=K)
     wl.group_size = gs
