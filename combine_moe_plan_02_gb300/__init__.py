@@ -279,7 +279,7 @@ def moe_dispatch_dedup(x: torch.Tensor, gp: GroupPlan, *, packed_x: Optional[tor
         packed_x = torch.empty(S * K, H, dtype=x.dtype, device=x.device)
     _abi.check("moe_dispatch_dedup", lib().moe_dispatch_dedup(
         _ptr(x), S, H, _dt(x), K, gp.G, _ptr(gp.goff), _ptr(gp.grp_src), _ptr(gp.grp_tok_map),
-        gp.max_rows, _ptr(grp_x), _ptr(packed_x), _stream(stream)))
+        _ptr(gp.gtok_map), gp.max_rows, _ptr(grp_x), _ptr(packed_x), _stream(stream)))
     return grp_x, packed_x
 
 

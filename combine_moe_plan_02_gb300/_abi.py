@@ -30,7 +30,7 @@ SIGNATURES = {
     "moe_group_plan_workspace_size": (SZ, [I64, I32, I32, I32]),
     "moe_group_plan": (I32, [P, P, I64, I32, I32, I32, P, P, P, P, P, P, SZ, P]),
     "moe_dispatch": (I32, [P, I64, I64, I32, I32, P, P, I64, P, I64, P, P]),
-    "moe_dispatch_dedup": (I32, [P, I64, I64, I32, I32, I32, P, P, P, I64, P, P, P]),
+    "moe_dispatch_dedup": (I32, [P, I64, I64, I32, I32, I32, P, P, P, P, I64, P, P, P]),
     "moe_dispatch_quant_fp8": (I32, [P, I64, I64, I32, P, I32, P, P, I64, P]),
     "moe_combine": (I32, [P, I64, I32, P, P, I64, I64, I32, P, I32, P]),
     "moe_combine_dedup": (I32, [P, I32, P, P, I32, P, P, P, I64, I64, I32, I64, P, P, I32, P]),

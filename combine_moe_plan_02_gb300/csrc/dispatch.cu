@@ -100,6 +100,11 @@ struct CopyArgs {
     int stage_bytes;           // chunk + scale area, multiple of 128
     uint8_t *dst2;             // with dst_map and K < 32: lane K also stores item row r here
     int64_t dst2_rows;         // rows of dst2 (bounds check)
+    // dedup by token (2K <= 32): item row r is token r; lanes K..2K-1 store
+    // to its group rows gtok_map[r, k] in dst2, lanes 0..K-1 to the packed
+    // rows read from grp_map (the group rows' expert maps)
+    const int64_t *gtok_map;   // [rows, K] or null
+    const int64_t *grp_map;    // [dst2_rows, K]
 };
 
 __global__ void __launch_bounds__(kWarpsPerCta * 32) dispatch_bulk_kernel(CopyArgs a)
@@ -157,12 +162,36 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) dispatch_bulk_kernel(CopyAr
             }
         }
         int64_t d = -1;
-        const bool second = a.dst2 != nullptr && lane == a.K;  // the item's own copy
-        if (a.dst_map) {
-            if (lane < a.K) d = __ldg(a.dst_map + r * a.K + lane);
-            else if (second) d = r;
-        } else if (lane == 0) {
-            d = r;
+        bool second;  // this lane stores to dst2
+        if (a.gtok_map) {
+            second = lane >= a.K && lane < 2 * a.K;
+            int64_t gk = -1;  // lane k < K: the token's group row through entry k
+            if (lane < a.K) {
+                gk = __ldg(a.gtok_map + r * a.K + lane);
+                if (gk < -1 || gk >= a.dst2_rows) {
+                    atomicOr(&g_dispatch_error, kErrDispatchIndex);
+                    gk = -1;
+                }
+            }
+            // lane k < K: its packed row, from the map of the group row that
+            // holds entry k (one load per group row of the token)
+            for (unsigned m = __ballot_sync(0xffffffffu, gk >= 0); m; m &= m - 1) {
+                const int64_t rq = __shfl_sync(0xffffffffu, gk, __ffs(m) - 1);
+                if (lane < a.K) {
+                    const int64_t e = __ldg(a.grp_map + rq * a.K + lane);
+                    if (e != -1) d = e;
+                }
+            }
+            const int64_t g2 = __shfl_sync(0xffffffffu, gk, (lane - a.K) & 31);
+            if (second) d = g2;
+        } else {
+            second = a.dst2 != nullptr && lane == a.K;  // the item's own copy
+            if (a.dst_map) {
+                if (lane < a.K) d = __ldg(a.dst_map + r * a.K + lane);
+                else if (second) d = r;
+            } else if (lane == 0) {
+                d = r;
+            }
         }
         const int64_t lim = second ? a.dst2_rows : a.dst_rows;
         if (d >= lim || d < -1 || (d >= 0 && !src_ok)) {
@@ -200,7 +229,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) dispatch_bulk_kernel(CopyAr
             const uint8_t *stage = ring + (size_t)st * a.stage_bytes;
             const int64_t d = dst_row[st];
             if (d >= 0) {
-                if (a.dst2 != nullptr && lane == a.K) {
+                if (a.gtok_map ? lane >= a.K : (a.dst2 != nullptr && lane == a.K)) {
                     bulk_s2g(a.dst2 + d * a.row_bytes + off, stage, bytes);
                 } else {
                     bulk_s2g(a.dst + d * a.row_bytes + off, stage, bytes);
@@ -627,13 +656,15 @@ MOE_EXPORT int moe_dispatch(const void *x, int64_t S, int64_t H, int dtype, int 
 
 MOE_EXPORT int moe_dispatch_dedup(const void *x, int64_t S, int64_t H, int dtype, int K, int G,
                                   const int64_t *goff, const int32_t *grp_src,
-                                  const int64_t *grp_tok_map, int64_t max_rows, void *grp_x,
-                                  void *packed_x, moe_stream_t stream)
+                                  const int64_t *grp_tok_map, const int64_t *gtok_map,
+                                  int64_t max_rows, void *grp_x, void *packed_x,
+                                  moe_stream_t stream)
 {
     const int es = elem_size(dtype);
     if (es == 0 || S < 0 || H < 1 || K < 1 || K > 32 || G < 1 || G > 1024) return MOE_EINVAL;
     if (S == 0) return MOE_OK;
-    if (!x || !goff || !grp_src || !grp_tok_map || !grp_x || !packed_x) return MOE_EINVAL;
+    if (!x || !goff || !grp_src || !grp_tok_map || !gtok_map || !grp_x || !packed_x)
+        return MOE_EINVAL;
     if (max_rows < S * (int64_t)(K < G ? K : G)) return MOE_EINVAL;
     const int64_t row_bytes = H * es;
     if (row_bytes % 16 || !aligned16(x) || !aligned16(grp_x) || !aligned16(packed_x))
@@ -641,6 +672,22 @@ MOE_EXPORT int moe_dispatch_dedup(const void *x, int64_t S, int64_t H, int dtype
     CopyArgs a = {};
     a.row_bytes = row_bytes;
     a.chunk = pick_chunk(row_bytes, &a.n_chunks);
+    if (2 * K <= 32) {
+        // by token: each chunk of x[s] is staged once and stored to the
+        // token's group rows and to its experts' packed rows
+        a.src = static_cast<const uint8_t *>(x);
+        a.rows = S;
+        a.src_rows = S;
+        a.src_div = 1;
+        a.dst = static_cast<uint8_t *>(packed_x);
+        a.K = K;
+        a.dst_rows = S * (int64_t)K;
+        a.dst2 = static_cast<uint8_t *>(grp_x);
+        a.dst2_rows = max_rows;
+        a.gtok_map = gtok_map;
+        a.grp_map = grp_tok_map;
+        return launch_copy(a, (cudaStream_t)stream);
+    }
     a.rows = max_rows;
     a.rows_dev = goff + G;
     if (K < 32) {

@@ -212,15 +212,26 @@ struct GroupKey {
     }
     __device__ __forceinline__ int chunk_key(int64_t i, bool in_range) const
     {
-        int g = in_range ? group(i) : -1;
+        return chunk_key_g(i, in_range, in_range ? group(i) : -1);
+    }
+    // chunk_key with the entry's group already loaded (g = -1 when i is past
+    // the end or its expert is invalid)
+    __device__ __forceinline__ int chunk_key_g(int64_t i, bool in_range, int g) const
+    {
         const int lane = threadIdx.x & 31;
         if ((32 % K) == 0) {
             // Chunks start at multiples of 32, so a token's K entries sit in
-            // one chunk: ballot dedup over (token, group) inside the warp.
-            const int tok = lane / K;
-            unsigned peers = __match_any_sync(0xffffffffu, g < 0 ? -1 - lane : tok * 4096 + g);
+            // one chunk: an entry represents its group unless an earlier lane
+            // of the same token holds the same group (K - 1 shuffles; a
+            // match per chunk costs far more on this part)
+            const int base = lane - lane % K;
+            bool rep = g >= 0;
+            for (int kk = 0; kk < K - 1; ++kk) {
+                const int v = __shfl_sync(0xffffffffu, g, base + kk);
+                if (kk < lane - base && v == g) rep = false;
+            }
             if (!in_range) return -2;
-            return (g >= 0 && lane == __ffs(peers) - 1) ? g : -1;
+            return rep ? g : -1;
         }
         if (!in_range) return -2;
         if (g < 0) return -1;
@@ -268,21 +279,36 @@ struct GroupKey {
     {
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
         const int G = E / gs;
+        // the groups of kPre chunks are loaded before any of them is keyed,
+        // so the loads of a warp overlap instead of queueing one by one
+        constexpr int kPre = 8;
+        const int64_t cstride = (int64_t)kWarps * 32;
         if (G <= 32) {
             // lane g tallies group g in registers (one ballot per group and
             // chunk), then adds once: no contended shared-memory atomics
             int bef = 0, aft = 0;
-            for (int64_t c = (int64_t)warp * 32; c < n; c += (int64_t)kWarps * 32) {
-                const int64_t i = c + lane;
-                const int k = chunk_key(i, i < n);
-                const bool before = c < tile_begin;
-                for (int gg = 0; gg < G; ++gg) {
-                    const int cnt = __popc(__ballot_sync(0xffffffffu, k == gg));
-                    if (lane == gg) {
-                        if (before)
-                            bef += cnt;
-                        else
-                            aft += cnt;
+            for (int64_t c0 = (int64_t)warp * 32; c0 < n; c0 += cstride * kPre) {
+                int gv[kPre];
+#pragma unroll
+                for (int q = 0; q < kPre; ++q) {
+                    const int64_t i = c0 + q * cstride + lane;
+                    gv[q] = i < n ? group(i) : -1;
+                }
+#pragma unroll
+                for (int q = 0; q < kPre; ++q) {
+                    const int64_t c = c0 + q * cstride;
+                    if (c >= n) break;  // the same for every lane
+                    const int64_t i = c + lane;
+                    const int k = chunk_key_g(i, i < n, gv[q]);
+                    const bool before = c < tile_begin;
+                    for (int gg = 0; gg < G; ++gg) {
+                        const int cnt = __popc(__ballot_sync(0xffffffffu, k == gg));
+                        if (lane == gg) {
+                            if (before)
+                                bef += cnt;
+                            else
+                                aft += cnt;
+                        }
                     }
                 }
             }
@@ -292,12 +318,22 @@ struct GroupKey {
             }
             return 0;
         }
-        for (int64_t c = (int64_t)warp * 32; c < n; c += (int64_t)kWarps * 32) {
-            const int64_t i = c + lane;
-            const int k = chunk_key(i, i < n);
-            const unsigned peers = __match_any_sync(0xffffffffu, k);
-            if (k >= 0 && lane == __ffs(peers) - 1) {
-                atomicAdd(c < tile_begin ? &s_bef[k] : &s_tot[k], __popc(peers));
+        for (int64_t c0 = (int64_t)warp * 32; c0 < n; c0 += cstride * kPre) {
+            int gv[kPre];
+#pragma unroll
+            for (int q = 0; q < kPre; ++q) {
+                const int64_t i = c0 + q * cstride + lane;
+                gv[q] = i < n ? group(i) : -1;
+            }
+#pragma unroll
+            for (int q = 0; q < kPre; ++q) {
+                const int64_t c = c0 + q * cstride;
+                if (c >= n) break;  // the same for every lane
+                const int64_t i = c + lane;
+                const int k = chunk_key_g(i, i < n, gv[q]);
+                const unsigned peers = __match_any_sync(0xffffffffu, k);
+                if (k >= 0 && lane == __ffs(peers) - 1)
+                    atomicAdd(c < tile_begin ? &s_bef[k] : &s_tot[k], __popc(peers));
             }
         }
         return 0;

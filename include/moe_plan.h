@@ -282,16 +282,19 @@ int moe_plan_dispatch(const int32_t *topk_idx, const void *x, int64_t S, int64_t
  * per (received token, k)].  Writes, on `stream`:
  *   grp_x[r, :]                = x[grp_src[r] / K, :]          r < R = goff[G]
  *   packed_x[grp_tok_map[r,k]] = grp_x[r, :]      for grp_tok_map[r,k] >= 0
- * For K < 32 both come from one pass (each chunk of the source row is staged
- * once and stored to the group row and to its experts' packed rows); K = 32
- * takes two passes, the second reading grp_x.
+ * gtok_map (moe_group_plan) gives each token's group rows.  For K <= 16 one
+ * pass walks tokens: each chunk of x[s] is staged once and stored to the
+ * token's group rows and to its experts' packed rows, so x is read once; for
+ * 16 < K < 32 one pass walks group rows (x[s] is read once per group row);
+ * K = 32 takes two passes, the second reading grp_x.
  * max_rows: rows allocated for grp_x (and grp_src/grp_tok_map); must be at
  * least S * min(K, G), which bounds R.  Alignment as moe_dispatch.
  * ---------------------------------------------------------------------- */
 int moe_dispatch_dedup(const void *x, int64_t S, int64_t H, int dtype, int K, int G,
                        const int64_t *goff, const int32_t *grp_src,
-                       const int64_t *grp_tok_map, int64_t max_rows, void *grp_x,
-                       void *packed_x, moe_stream_t stream);
+                       const int64_t *grp_tok_map, const int64_t *gtok_map,
+                       int64_t max_rows, void *grp_x, void *packed_x,
+                       moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Combine  [mori #448: PR description (gather each token's k expert outputs,

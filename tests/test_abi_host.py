@@ -86,9 +86,11 @@ def test_dispatch_validation(L):
     assert d(px=MIS) == EALIGN
     assert d(ns=48) == EINVAL                # scales without buffers
     assert d(ns=3, xs=FAKE, ps=FAKE) == EALIGN   # 12-byte scale rows
-    assert L.moe_dispatch_dedup(FAKE, 16, 64, 0, 8, 8, FAKE, FAKE, FAKE, 100, FAKE, FAKE,
+    assert L.moe_dispatch_dedup(FAKE, 16, 64, 0, 8, 8, FAKE, FAKE, FAKE, FAKE, 100, FAKE, FAKE,
                                 None) == EINVAL  # max_rows < S*min(K,G)
-    assert L.moe_dispatch_dedup(FAKE, 16, 64, 0, 8, 8, FAKE, FAKE, FAKE, 128, MIS, FAKE,
+    assert L.moe_dispatch_dedup(FAKE, 16, 64, 0, 8, 8, FAKE, FAKE, FAKE, None, 128, FAKE, FAKE,
+                                None) == EINVAL  # no gtok_map
+    assert L.moe_dispatch_dedup(FAKE, 16, 64, 0, 8, 8, FAKE, FAKE, FAKE, FAKE, 128, MIS, FAKE,
                                 None) == EALIGN
 
 
