@@ -279,6 +279,47 @@ struct GroupKey {
     {
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
         const int G = E / gs;
+        if (G <= 8) {
+            // one token per thread: its representatives are found by comparing
+            // its K groups, and counted in 8-bit fields of two registers (a
+            // thread sees at most n / K / kThreads < 256 tokens here), then
+            // summed over the warp and added once per group
+            uint64_t pb = 0, pa = 0;
+            const int64_t ntok = n / K;
+            for (int64_t t = threadIdx.x; t < ntok; t += kThreads) {
+                int gv[32];
+#pragma unroll
+                for (int kk = 0; kk < 32; ++kk)
+                    if (kk < K) gv[kk] = group(t * K + kk);
+#pragma unroll
+                for (int kk = 0; kk < 32; ++kk) {
+                    if (kk >= K) break;
+                    bool rep = gv[kk] >= 0;
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj)
+                        if (jj < kk && gv[jj] == gv[kk]) rep = false;
+                    if (rep) {
+                        const uint64_t one = 1ull << (8 * gv[kk]);
+                        if (t * K + kk < tile_begin)
+                            pb += one;
+                        else
+                            pa += one;
+                    }
+                }
+            }
+            for (int gg = 0; gg < G; ++gg) {
+                int b = (int)((pb >> (8 * gg)) & 0xff), f = (int)((pa >> (8 * gg)) & 0xff);
+                for (int o = 16; o; o >>= 1) {
+                    b += __shfl_xor_sync(0xffffffffu, b, o);
+                    f += __shfl_xor_sync(0xffffffffu, f, o);
+                }
+                if (lane == 0) {
+                    if (b) atomicAdd(&s_bef[gg], b);
+                    if (f) atomicAdd(&s_tot[gg], f);
+                }
+            }
+            return 0;
+        }
         // the groups of kPre chunks are loaded before any of them is keyed,
         // so the loads of a warp overlap instead of queueing one by one
         constexpr int kPre = 8;
