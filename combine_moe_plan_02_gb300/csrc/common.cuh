@@ -142,22 +142,6 @@ __device__ __forceinline__ uint32_t lanemask_lt()
     return m;
 }
 
-// For each lane: how many lower lanes hold the same key, and how many lanes
-// of the warp hold it -- the stable rank and the group size that
-// __match_any_sync + popc would give, from 32 shuffles.  All lanes call it.
-__device__ __forceinline__ void warp_same_key(int key, int &below, int &total)
-{
-    const int lane = threadIdx.x & 31;
-    below = 0;
-    total = 0;
-#pragma unroll
-    for (int l = 0; l < 32; ++l) {
-        const int eq = __shfl_sync(0xffffffffu, key, l) == key;
-        total += eq;
-        below += (l < lane) ? eq : 0;
-    }
-}
-
 // mbarrier ------------------------------------------------------------------
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)

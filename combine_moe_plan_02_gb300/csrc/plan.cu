@@ -222,8 +222,7 @@ struct GroupKey {
         if ((32 % K) == 0) {
             // Chunks start at multiples of 32, so a token's K entries sit in
             // one chunk: an entry represents its group unless an earlier lane
-            // of the same token holds the same group (K - 1 shuffles; a
-            // match per chunk costs far more on this part)
+            // of the same token holds the same group (K - 1 shuffles)
             const int base = lane - lane % K;
             bool rep = g >= 0;
             for (int kk = 0; kk < K - 1; ++kk) {

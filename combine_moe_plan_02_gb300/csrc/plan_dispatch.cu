@@ -32,10 +32,6 @@ constexpr int kSeg = 512;       // bytes of a row segment copied by one warp
 #endif
 constexpr int64_t kFusedMaxEntries = MOE_PLAN_DISPATCH_FUSED_MAX;
 
-#ifndef MOE_PD_MATCH
-#define MOE_PD_MATCH 0
-#endif
-
 __device__ uint32_t g_pd_error;  // kErrDispatchIndex
 
 struct PDArgs {
@@ -137,14 +133,8 @@ __global__ void __launch_bounds__(kThreads, 1) plan_dispatch_kernel(PDArgs a)
         const int64_t i = c + lane;
         const int k = entry_key(a, i, i < wend);
         if (k == -1) ++invalid;
-#if MOE_PD_MATCH
         const unsigned peers = __match_any_sync(0xffffffffu, k);
         if (k >= 0 && lane == __ffs(peers) - 1) my_wc[k] += __popc(peers);
-#else
-        int below, total;
-        warp_same_key(k, below, total);
-        if (k >= 0 && below == 0) my_wc[k] += total;
-#endif
         __syncwarp();
     }
     for (int sh = 16; sh; sh >>= 1) invalid += __shfl_xor_sync(0xffffffffu, invalid, sh);
@@ -186,13 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1) plan_dispatch_kernel(PDArgs a)
     for (int64_t c = wbegin; c < wend; c += 32) {
         const int64_t i = c + lane;
         const int k = entry_key(a, i, i < wend);
-#if MOE_PD_MATCH
         const unsigned peers = __match_any_sync(0xffffffffu, k);
         const int below = __popc(peers & lanemask_lt()), total = __popc(peers);
-#else
-        int below, total;
-        warp_same_key(k, below, total);
-#endif
         int32_t row = -1;
         if (k >= 0) row = s_off[k] + my_wc[k] + below;
         __syncwarp();
