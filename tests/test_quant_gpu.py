@@ -97,6 +97,30 @@ def test_edge_rows():
 
 
 @pytest.mark.timeout(600)
+@pytest.mark.parametrize("H", [1024, 384])   # shared-memory kernel, register kernel
+def test_tiny_blocks(H):
+    """Blocks whose largest magnitude is near or below 2^-83, down to the
+    smallest bf16 subnormal: their scale amax/448 reaches the f32 subnormal
+    range, where the reciprocal-based division is not exact; the codes and
+    scales must still be those of the oracle's plain divisions."""
+    rng = np.random.default_rng(5)
+    S, E, K = 64, 8, 3
+    mags = [2.0 ** -82, 2.0 ** -83, 2.0 ** -84, 1e-30, 1e-35, 5.3e-36, 1e-37, 1e-38,
+            2.0 ** -126, 2.0 ** -127, 2.0 ** -130, 2.0 ** -133]
+    xf = np.zeros((S, H), np.float32)
+    nb = H // 128
+    for r in range(S):
+        for b in range(nb):
+            m = mags[(r * nb + b) % len(mags)]
+            blk = rng.standard_normal(128).astype(np.float32) * np.float32(m)
+            blk[rng.integers(0, 128)] = np.float32(m) * (1 if (r + b) % 2 else -1)
+            xf[r, b * 128:(b + 1) * 128] = blk
+    x = workloads.to_bf16_bits(xf)
+    idx = workloads.topk_uniform(9, S, E, K)
+    _check(x, idx, E, 128)
+
+
+@pytest.mark.timeout(600)
 def test_every_bf16_value_encodes_like_the_oracle():
     """Each 128-block holds 448 (so scale = 1 and the codes are the plain
     E4M3 encoding of the inputs) and 127 bf16 values; together the rows cover
