@@ -297,6 +297,10 @@ struct QuantArgs {
     float *scales;            // [dst_rows, H / block]
 };
 
+// IEEE division, kept out of line: only blocks of tiny values take it, and
+// inlined it would crowd the registers of the common path.
+__device__ __noinline__ float div_rn_out_of_line(float a, float b) { return __fdiv_rn(a, b); }
+
 // Quantises the 8 bf16 values of one lane (one 16-byte word) for a block of
 // GL lanes: returns the 8 E4M3 codes (little-endian in two words) and the
 // block's scale.  All 32 lanes must call it together (block amax shuffle).
@@ -318,15 +322,29 @@ __device__ __forceinline__ uint2 quant8(const uint4 v, bool active, float &scale
 #pragma unroll
     for (int o = GL / 2; o > 0; o >>= 1)
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-    // v / scale, correctly rounded, by Markstein's correction step
-    // (P. Markstein, IBM J. Res. Dev. 34(1), 1990): with y = RN(1/scale)
-    // and q = RN(v*y), the residual v - q*scale is exact under FMA and
-    // RN(q + residual*y) = RN(v/scale).  One reciprocal per block
-    // instead of a full division per element.  A zero residual means
-    // q0 is the exact quotient; returning it keeps the sign of -0.
+    // Divisions, correctly rounded, by Markstein's correction step
+    // (P. Markstein, IBM J. Res. Dev. 34(1), 1990): with y = RN(1/b) and
+    // q = RN(a*y), the residual a - q*b is exact under FMA and
+    // RN(q + residual*y) = RN(a/b).  The residual is exact only while a is
+    // at least 2^-102 (24 bits above the subnormal range); a block whose
+    // amax is below 2^-83 can hold elements that small with quotients that
+    // still reach an E4M3 code, so such blocks take full divisions instead.
+    constexpr float kInv448 = 1.0f / 448.0f;  // RN(1/448)
+    const bool exact_fast = amax >= 0x1p-83f;
+    float scale = 1.0f;
+    if (exact_fast) {
+        const float q0 = __fmul_rn(amax, kInv448);
+        scale = __fmaf_rn(__fmaf_rn(-q0, 448.0f, amax), kInv448, q0);
+    } else if (amax > 0.0f) {
+        scale = div_rn_out_of_line(amax, 448.0f);
+    }
+    // one reciprocal per block instead of a full division per element; a
+    // zero residual means q0 is the exact quotient, and returning it keeps
+    // the sign of -0
     const float y = __frcp_rn(scale);
+    const bool slow = amax > 0.0f && !exact_fast;
     auto quot = [&](float x) {
+        if (slow) return div_rn_out_of_line(x, scale);
         const float q0 = __fmul_rn(x, y);
         const float r = __fmaf_rn(-q0, scale, x);
         return r == 0.0f ? q0 : __fmaf_rn(r, y, q0);

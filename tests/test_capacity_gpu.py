@@ -91,3 +91,27 @@ def test_capacity_with_invalid_ids():
     idx[::4, 1] = -1
     idx[::9, 3] = 99
     _check(wl, idx, 60)
+
+
+def test_plan_replay_with_new_rows():
+    """Routing-handle replay (mori #448, routing-handle note): one plan, then
+    dispatch and combine of a second batch of rows with the same routing;
+    both passes match the oracle run on their own rows."""
+    import combine_moe_plan_02_gb300 as moe
+    wl = workloads.make("moonep", seed=71, S=333, H=1032, E=64, K=8)
+    wl2 = workloads.make("moonep", seed=72, S=333, H=1032, E=64, K=8)
+    dev = torch.device("cuda")
+    plan = moe.moe_plan(torch.from_numpy(wl.topk_idx).to(dev), wl.E)
+    w = torch.from_numpy(wl.topk_w).to(dev)
+    p = oracle.plan(wl.topk_idx, wl.E)
+    for rows in (wl.x, wl2.x, wl.x):
+        x = torch.from_numpy(rows.view(np.int16)).to(dev).view(torch.bfloat16)
+        packed = gpu_path.poisoned((wl.S * wl.K, wl.H), torch.bfloat16)
+        moe.moe_dispatch(x, plan.tok_map, packed_x=packed)
+        out = moe.moe_combine(packed, w, plan.tok_map)
+        torch.cuda.synchronize()
+        ref_packed = oracle.dispatch(rows, p["tok_map"], wl.S * wl.K)
+        assert np.array_equal(gpu_path._np(packed), ref_packed)
+        ref_out = oracle.combine(ref_packed, "bf16", wl.topk_w, p["tok_map"], wl.H, "bf16")
+        assert np.array_equal(gpu_path._np(out), ref_out)
+    assert moe.moe_device_errors() == 0

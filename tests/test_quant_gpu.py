@@ -166,3 +166,29 @@ def test_quantised_dispatch_matches_dispatch_of_quantised_rows():
     torch.cuda.synchronize()
     assert torch.equal(pq.view(torch.uint8), fq.view(torch.uint8))
     assert torch.equal(ps.view(torch.int32), fs.view(torch.int32))
+
+
+@pytest.mark.timeout(600)
+def test_full_size_sampled_tokens():
+    """The benchmarked launch (S=4096 H=7168 E=64 K=8, block 128), checked on
+    a sample of 96 tokens: quantisation is per token row, so the oracle
+    quantises just those rows and each of their K packed rows must match."""
+    import combine_moe_plan_02_gb300 as moe
+    wl = workloads.make("moonep", seed=0)
+    dev = torch.device("cuda")
+    x = torch.from_numpy(wl.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    plan = moe.moe_plan(torch.from_numpy(wl.topk_idx).to(dev), wl.E)
+    q, sc = moe.moe_dispatch_quant_fp8(x, plan.tok_map)
+    torch.cuda.synchronize()
+    assert moe.moe_device_errors() == 0
+    tm = plan.tok_map.cpu().numpy()
+    assert np.array_equal(tm, oracle.plan(wl.topk_idx, wl.E)["tok_map"])
+    sample = np.sort(np.random.default_rng(0).choice(wl.S, 96, replace=False))
+    q0, sc0 = oracle.quant_fp8(np.ascontiguousarray(wl.x[sample]), 128)
+    qn = q.view(torch.uint8).cpu().numpy()
+    scn = sc.cpu().numpy()
+    for j, s in enumerate(sample):
+        for k in range(wl.K):
+            r = tm[s, k]
+            assert np.array_equal(qn[r], q0[j]), (s, k)
+            assert np.array_equal(scn[r].view(np.uint32), sc0[j].view(np.uint32)), (s, k)
