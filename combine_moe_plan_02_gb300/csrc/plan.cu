@@ -156,22 +156,6 @@ struct DirectKey {
         };
         int invalid = 0;
         int64_t done = 0;
-#ifdef MOE_PLAN_COUNT_MATCH
-        // warp-aggregated: lanes holding the same expert add once
-        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        for (int64_t c = (int64_t)warp * 32; c < n; c += (int64_t)kWarps * 32) {
-            const int64_t i = c + lane;
-            int e = i < n ? __ldg(idx + i) : -1;
-            const bool valid = e >= 0 && e < E;
-            if (!valid && i < n) ++invalid;
-            const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1 - lane);
-            if (valid && lane == __ffs(peers) - 1) {
-                atomicAdd(c < tile_begin ? &s_bef[e] : &s_aft[e], __popc(peers));
-                if (int32_t *wc = wc_row(c)) atomicAdd(&wc[e], __popc(peers));
-            }
-        }
-        return invalid;
-#endif
         if ((reinterpret_cast<uintptr_t>(idx) & 15u) == 0) {
             const int4 *p = reinterpret_cast<const int4 *>(idx);
             const int64_t n4 = n / 4;
