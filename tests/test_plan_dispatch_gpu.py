@@ -120,3 +120,38 @@ def test_empty_batch():
     plan, _, _ = moe.moe_plan_dispatch(idx, x, 16)
     torch.cuda.synchronize()
     assert plan.cnt.sum().item() == 0 and plan.off.sum().item() == 0
+
+
+@pytest.mark.parametrize("S", [16, 600])
+def test_cuda_graph_replay(S):
+    """Plan, dispatch and combine captured once into a CUDA graph (one fused
+    launch at 16 tokens, two calls at 600) and replayed on new inputs copied
+    into the captured buffers: every replay matches the oracle."""
+    import combine_moe_plan_02_gb300 as moe
+    dev = torch.device("cuda")
+    wls = [workloads.make("moonep", seed=80 + r, S=S, H=1032, E=64, K=8) for r in range(3)]
+    wl = wls[0]
+    idx = torch.from_numpy(wl.topk_idx).to(dev)
+    w = torch.from_numpy(wl.topk_w).to(dev)
+    x = torch.from_numpy(wl.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        plan, px, _ = moe.moe_plan_dispatch(idx, x, wl.E, stream=stream)
+        out = moe.moe_combine(px, w, plan.tok_map, stream=stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            moe.moe_plan_dispatch(idx, x, wl.E, out=plan, packed_x=px, stream=stream)
+            moe.moe_combine(px, w, plan.tok_map, out=out, stream=stream)
+    for v in wls[1:] + wls[:1]:
+        idx.copy_(torch.from_numpy(v.topk_idx))
+        w.copy_(torch.from_numpy(v.topk_w))
+        x.view(torch.int16).copy_(torch.from_numpy(v.x.view(np.int16)))
+        g.replay()
+        torch.cuda.synchronize()
+        p = oracle.plan(v.topk_idx, v.E)
+        assert np.array_equal(np_(plan.tok_map), p["tok_map"])
+        opk = oracle.dispatch(v.x, p["tok_map"], v.S * v.K)
+        ref = oracle.combine(opk, "bf16", v.topk_w, p["tok_map"], v.H, "bf16")
+        assert np.array_equal(np_(out), ref)
+    assert moe.moe_device_errors() == 0
