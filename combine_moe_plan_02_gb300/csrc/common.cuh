@@ -81,6 +81,7 @@ cudaError_t prepare_kernel(F fn, size_t smem, int threads, KernelCache &kc, int 
         if (e != cudaSuccess) return e;
         if (cached) kc.smem_limit[dev] = (int)smem;
     }
+
     if (per_sm) {
         if (cached && kc.occ_smem[dev] == (int)smem + 1) {
             *per_sm = kc.occ[dev];
@@ -110,7 +111,10 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+#ifndef MOE_USE_PDL
+#define MOE_USE_PDL 1
+#endif
+    attr[0].val.programmaticStreamSerializationAllowed = MOE_USE_PDL;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);

@@ -141,14 +141,33 @@ struct DirectKey {
         }
     }
 
+    // The first kPre 16-byte groups of this thread in the all-entries pass,
+    // loaded at kernel start so that their latency overlaps the set-up.
+    static constexpr int kPre = 8;
+    struct Pre {
+        int4 v[kPre];
+    };
+    __device__ __forceinline__ void prefetch(int64_t n, Pre &pre) const
+    {
+        if ((reinterpret_cast<uintptr_t>(idx) & 15u) != 0) return;
+        const int4 *p = reinterpret_cast<const int4 *>(idx);
+        const int64_t n4 = n / 4;
+#pragma unroll
+        for (int u = 0; u < kPre; ++u) {
+            const int64_t q = threadIdx.x + (int64_t)u * kThreads;
+            if (q < n4) pre.v[u] = __ldg(p + q);
+        }
+    }
+
     // Counts all n entries: those before `tile_begin` (a multiple of 1024)
     // into s_bef, the others into s_aft, and those of this tile [tile_begin,
     // tile_end) also into their warp sub-tile's row of s_wc.  Returns this
     // thread's invalid entries.  Each thread takes 16-byte groups of 4
-    // entries (always inside one sub-tile), four groups in flight.
+    // entries (always inside one sub-tile): first the kPre prefetched ones,
+    // then the rest four in flight.
     __device__ __forceinline__ int count_all(int64_t n, int64_t tile_begin, int64_t tile_end,
                                              int64_t sub, int wstride, int32_t *s_aft,
-                                             int32_t *s_bef, int32_t *s_wc) const
+                                             int32_t *s_bef, int32_t *s_wc, const Pre &pre) const
     {
         auto wc_row = [&](int64_t j) -> int32_t * {
             return (j >= tile_begin && j < tile_end) ? s_wc + ((j - tile_begin) / sub) * wstride
@@ -159,7 +178,20 @@ struct DirectKey {
         if ((reinterpret_cast<uintptr_t>(idx) & 15u) == 0) {
             const int4 *p = reinterpret_cast<const int4 *>(idx);
             const int64_t n4 = n / 4;
-            for (int64_t q0 = threadIdx.x; q0 < n4; q0 += 4 * kThreads) {
+#pragma unroll
+            for (int u = 0; u < kPre; ++u) {
+                const int64_t q = threadIdx.x + (int64_t)u * kThreads;
+                if (q < n4) {
+                    const bool before = q * 4 < tile_begin;
+                    int32_t *wc = wc_row(q * 4);
+                    add(pre.v[u].x, before, wc, s_aft, s_bef, invalid);
+                    add(pre.v[u].y, before, wc, s_aft, s_bef, invalid);
+                    add(pre.v[u].z, before, wc, s_aft, s_bef, invalid);
+                    add(pre.v[u].w, before, wc, s_aft, s_bef, invalid);
+                }
+            }
+            for (int64_t q0 = threadIdx.x + (int64_t)kPre * kThreads; q0 < n4;
+                 q0 += 4 * kThreads) {
                 int4 v[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
@@ -253,12 +285,16 @@ struct GroupKey {
 
     static constexpr bool kMergesWarpCounts = false;
 
+    struct Pre {};
+    __device__ __forceinline__ void prefetch(int64_t, Pre &) const {}
+
     // Counts the representatives among all n entries (warp chunks of 32, so
     // that the ballot dedup sees whole tokens); chunks lie wholly before or
     // wholly after `tile_begin`, a multiple of 1024.  Per-warp counts of the
     // own tile come from step (a) instead.
     __device__ __forceinline__ int count_all(int64_t n, int64_t tile_begin, int64_t, int64_t,
-                                             int, int32_t *s_tot, int32_t *s_bef, int32_t *) const
+                                             int, int32_t *s_tot, int32_t *s_bef, int32_t *,
+                                             const Pre &) const
     {
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
         const int G = E / gs;
@@ -449,18 +485,22 @@ __global__ void __launch_bounds__(kThreads, 1) plan_rank_kernel(Key key, int nke
     // stream work finished, and topk_idx may be read before the wait.
     if (g.mode != kModeTwoKernel) griddep_wait();
 
-    for (int i = threadIdx.x; i < kWarps * wstride; i += kThreads) s_wc[i] = 0;
-    for (int i = threadIdx.x; i < nkeys; i += kThreads) s_tot[i] = s_bef[i] = 0;
-    if (threadIdx.x == 0) s_inval = 0;
-    __syncthreads();
-
     const int64_t wbegin = (int64_t)t * g.tile + (int64_t)warp * g.sub;
     const int64_t wend = min(wbegin + g.sub, g.n);
     int32_t *my_wc = s_wc + warp * wstride;
 
-    // keys of the warp's first chunk, fetched now so that their latency
-    // overlaps the counting; (a) and (e) reuse them
+    // first loads before anything else, so that their latency overlaps the
+    // clearing of shared memory: the keys of the warp's first chunk ((a) and
+    // (e) reuse them) and, in one-launch mode, the first groups of the
+    // all-entries pass
     const int k_first = key.chunk_key(wbegin + lane, wbegin + lane < wend);
+    typename Key::Pre pre;
+    if (g.mode == kModeFused) key.prefetch(g.n, pre);
+
+    for (int i = threadIdx.x; i < kWarps * wstride; i += kThreads) s_wc[i] = 0;
+    for (int i = threadIdx.x; i < nkeys; i += kThreads) s_tot[i] = s_bef[i] = 0;
+    if (threadIdx.x == 0) s_inval = 0;
+    __syncthreads();
     // in the one-launch mode the direct plan takes the per-warp counts of
     // its own tile from the all-entries pass in (b)
     const bool merged = g.mode == kModeFused && Key::kMergesWarpCounts;
@@ -494,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) plan_rank_kernel(Key key, int nke
         // s_tot collects the entries from this tile on, s_bef those before
         const int64_t tile_begin = (int64_t)t * g.tile;
         int inv = key.count_all(g.n, tile_begin, min(tile_begin + g.tile, g.n), g.sub, wstride,
-                                s_tot, s_bef, s_wc);
+                                s_tot, s_bef, s_wc, pre);
         if (Key::kCountsInvalid && t == 0) {
             for (int sh = 16; sh; sh >>= 1) inv += __shfl_xor_sync(0xffffffffu, inv, sh);
             if (lane == 0 && inv) atomicAdd(&s_inval, inv);
@@ -590,6 +630,11 @@ int run_plan(Key key, int nkeys, const PlanGeom &g, const RankOut &o, void *ws,
     if (need > 0 && (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOE_EALIGN;
     if (g.mode == kModeTwoKernel) {
         const size_t smem1 = (size_t)(nkeys + 1) * sizeof(int32_t);
+        static KernelCache hcache;  // one per Key instantiation
+        if (cudaError_t e = prepare_kernel(plan_hist_kernel<Key>, smem1, kThreads, hcache, nullptr)) {
+            set_cuda_error(e);
+            return MOE_ECUDA;
+        }
         plan_hist_kernel<Key><<<g.T, kThreads, smem1, stream>>>(key, nkeys, g,
                                                                  static_cast<int32_t *>(ws));
         if (int rc = check_launch()) return rc;

@@ -215,6 +215,231 @@ __global__ void __launch_bounds__(kThreads, 1) plan_dispatch_kernel(PDArgs a)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Larger batches: one launch with CTAs that own token ranges.  CTA c owns
+// the tpc tokens [c*tpc, (c+1)*tpc) (at most 1024 entries).  It counts all n
+// entries itself -- those before its range and the rest, per expert (16-byte
+// loads, shared-memory atomics) -- which gives the bucket offsets and the
+// counts of earlier tokens; ranks its own entries (one 32-entry chunk per
+// warp: __match_any_sync, a scan over warps per expert); writes their map and
+// packed_src entries; and then copies its own token rows to their packed
+// rows.  The copies of a CTA start as soon as its ranks are known, without a
+// kernel boundary between plan and dispatch; no CTA waits for another.
+// ---------------------------------------------------------------------------
+
+constexpr int kTilePre = 8;     // 16-byte index groups per thread loaded up front
+constexpr int kCopyUnroll = 4;  // row segments per warp with loads in flight
+
+__global__ void __launch_bounds__(kThreads, 1) plan_dispatch_tiles_kernel(PDArgs a, int64_t tpc)
+{
+    extern __shared__ int32_t smem[];
+    const int wstride = a.E | 1;
+    int32_t *s_wc = smem;                        // [kWarps][wstride] own-range per-warp counts
+    int32_t *s_bef = s_wc + kWarps * wstride;    // [E] entries before the range
+    int32_t *s_aft = s_bef + a.E;                // [E] the others
+    int32_t *s_base = s_aft + a.E;               // [E] first rank of the range per expert
+    int32_t *s_row = s_base + a.E;               // [tpc*K] packed row of each own entry
+    __shared__ int32_t s_scan[kWarps];
+    __shared__ int32_t s_inval;
+
+    griddep_wait();  // topk_idx and x come from earlier stream work
+    griddep_launch_dependents();
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const bool writer = blockIdx.x == 0;
+    const int64_t t0 = (int64_t)blockIdx.x * tpc;
+    const int64_t t1 = min(t0 + tpc, a.S);
+    const int64_t b0 = t0 * a.K, b1 = t1 * a.K;   // own entries [b0, b1)
+
+    // first loads: this warp's own chunk and the first index groups of the
+    // all-entries pass, so that their latency overlaps the set-up
+    const int64_t ci = b0 + warp * 32 + lane;
+    const int k_own = entry_key(a, ci, ci < b1);
+    const bool vec = (reinterpret_cast<uintptr_t>(a.idx) & 15u) == 0;
+    const int64_t n4 = vec ? a.n / 4 : 0;
+    const int4 *p4 = reinterpret_cast<const int4 *>(a.idx);
+    int4 pre[kTilePre];
+#pragma unroll
+    for (int u = 0; u < kTilePre; ++u) {
+        const int64_t q = threadIdx.x + (int64_t)u * kThreads;
+        if (q < n4) pre[u] = __ldg(p4 + q);
+    }
+
+    for (int i = threadIdx.x; i < kWarps * wstride; i += kThreads) s_wc[i] = 0;
+    for (int i = threadIdx.x; i < a.E; i += kThreads) s_bef[i] = s_aft[i] = 0;
+    if (threadIdx.x == 0) s_inval = 0;
+    __syncthreads();
+
+    // own-range per-warp counts (one chunk per warp)
+    {
+        const unsigned peers = __match_any_sync(0xffffffffu, k_own);
+        if (k_own >= 0 && lane == __ffs(peers) - 1) s_wc[warp * wstride + k_own] = __popc(peers);
+    }
+
+    // all entries: before the range -> s_bef, the rest -> s_aft
+    int invalid = 0;
+    auto add = [&](int e, int64_t i) {
+        if (e >= 0 && e < a.E)
+            atomicAdd(i < b0 ? &s_bef[e] : &s_aft[e], 1);
+        else
+            ++invalid;
+    };
+#pragma unroll
+    for (int u = 0; u < kTilePre; ++u) {
+        const int64_t q = threadIdx.x + (int64_t)u * kThreads;
+        if (q < n4) {
+            add(pre[u].x, 4 * q); add(pre[u].y, 4 * q + 1);
+            add(pre[u].z, 4 * q + 2); add(pre[u].w, 4 * q + 3);
+        }
+    }
+    for (int64_t q0 = threadIdx.x + (int64_t)kTilePre * kThreads; q0 < n4; q0 += 4 * kThreads) {
+        int4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (q0 + u * kThreads < n4) v[u] = __ldg(p4 + q0 + u * kThreads);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t q = q0 + u * kThreads;
+            if (q < n4) {
+                add(v[u].x, 4 * q); add(v[u].y, 4 * q + 1);
+                add(v[u].z, 4 * q + 2); add(v[u].w, 4 * q + 3);
+            }
+        }
+    }
+    for (int64_t i = n4 * 4 + threadIdx.x; i < a.n; i += kThreads) add(__ldg(a.idx + i), i);
+    if (writer) {
+        for (int sh = 16; sh; sh >>= 1) invalid += __shfl_xor_sync(0xffffffffu, invalid, sh);
+        if (lane == 0 && invalid) atomicAdd(&s_inval, invalid);
+    }
+    __syncthreads();
+
+    // totals, bucket offsets, the range's first rank per expert
+    const int e = threadIdx.x;
+    const int32_t bef = (e < a.E) ? s_bef[e] : 0;
+    const int32_t tot = (e < a.E) ? bef + s_aft[e] : 0;
+    int32_t total;
+    const int32_t offe = block_scan(tot, s_scan, total);
+    if (e < a.E) {
+        s_base[e] = offe + bef;
+        if (writer) {
+            a.cnt[e] = tot;
+            a.off[e] = offe;
+        }
+    }
+    if (writer && threadIdx.x == 0) {
+        a.off[a.E] = total;
+        *a.n_invalid = s_inval;
+    }
+    // per expert, exclusive scan over the warps of the range
+    for (int k = warp; k < a.E; k += kWarps) {
+        const int32_t c = s_wc[lane * wstride + k];
+        int32_t x = c;
+        for (int sh = 1; sh < 32; sh <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, x, sh);
+            if (lane >= sh) x += y;
+        }
+        s_wc[lane * wstride + k] = x - c;
+    }
+    __syncthreads();
+
+    // ranks of the own entries
+    {
+        const unsigned peers = __match_any_sync(0xffffffffu, k_own);
+        if (ci < b1) {
+            int32_t row = -1;
+            if (k_own >= 0)
+                row = s_base[k_own] + s_wc[warp * wstride + k_own] + __popc(peers & lanemask_lt());
+            s_row[ci - b0] = row;
+            a.map[ci] = row;
+            if (row >= 0) a.src[row] = (int32_t)ci;
+        }
+    }
+    __syncthreads();
+
+    // rows: unit = (own token, 512-byte segment), kCopyUnroll units per warp
+    // with their loads issued first
+    const int64_t per_tok = a.segs + a.ssegs;
+    const int64_t units = (t1 - t0) * per_tok;
+    for (int64_t u0 = (int64_t)warp * kCopyUnroll; u0 < units; u0 += (int64_t)kWarps * kCopyUnroll) {
+        uint4 v[kCopyUnroll];
+        int64_t tok[kCopyUnroll], obs[kCopyUnroll], len[kCopyUnroll];
+        bool is_row[kCopyUnroll], act[kCopyUnroll];
+#pragma unroll
+        for (int j = 0; j < kCopyUnroll; ++j) {
+            const int64_t u = u0 + j;
+            const int64_t tl = u / per_tok;
+            const int64_t g = u - tl * per_tok;
+            is_row[j] = g < a.segs;
+            len[j] = is_row[j] ? a.row_bytes : a.scale_bytes;
+            obs[j] = (is_row[j] ? g : g - a.segs) * kSeg + lane * 16;
+            tok[j] = tl;
+            act[j] = u < units && obs[j] < len[j];
+            if (act[j])
+                v[j] = ld_stream16((is_row[j] ? a.x : a.xs) + (t0 + tl) * len[j] + obs[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < kCopyUnroll; ++j) {
+            if (!act[j]) continue;
+            uint8_t *dst = is_row[j] ? a.px : a.ps;
+            for (int k = 0; k < a.K; ++k) {
+                const int32_t r = s_row[tok[j] * a.K + k];
+                if (r < 0) continue;
+                if (r < a.packed_rows)
+                    st16(dst + (int64_t)r * len[j] + obs[j], v[j]);
+                else
+                    atomicOr(&g_pd_error, kErrDispatchIndex);
+            }
+        }
+    }
+}
+
+#ifndef MOE_PD_TILED
+#define MOE_PD_TILED 1
+#endif
+constexpr int64_t kTiledMaxEntries = 131072;
+
+int launch_tiles(const int32_t *topk_idx, const void *x, int64_t S, int K, int E,
+                 int64_t row_bytes, const float *x_scales, int64_t n_scales, int32_t *cnt,
+                 int64_t *off, int32_t *packed_src, int64_t *tok_map, int32_t *n_invalid,
+                 void *packed_x, int64_t packed_rows, float *packed_scales, int64_t tpc,
+                 cudaStream_t stream)
+{
+    PDArgs a = {};
+    a.idx = topk_idx;
+    a.S = S;
+    a.K = K;
+    a.E = E;
+    a.n = S * (int64_t)K;
+    a.x = static_cast<const uint8_t *>(x);
+    a.row_bytes = row_bytes;
+    a.xs = reinterpret_cast<const uint8_t *>(x_scales);
+    a.scale_bytes = n_scales > 0 ? n_scales * 4 : 0;
+    a.segs = (row_bytes + kSeg - 1) / kSeg;
+    a.ssegs = (a.scale_bytes + kSeg - 1) / kSeg;
+    a.cnt = cnt;
+    a.off = off;
+    a.src = packed_src;
+    a.map = tok_map;
+    a.n_invalid = n_invalid;
+    a.px = static_cast<uint8_t *>(packed_x);
+    a.ps = reinterpret_cast<uint8_t *>(packed_scales);
+    a.packed_rows = packed_rows;
+    const size_t smem =
+        ((size_t)kWarps * (E | 1) + 3 * (size_t)E + (size_t)(tpc * K)) * sizeof(int32_t);
+    static KernelCache cache;
+    cudaError_t err = prepare_kernel(plan_dispatch_tiles_kernel, smem, kThreads, cache, nullptr);
+    if (err == cudaSuccess) {
+        const unsigned blocks = (unsigned)((S + tpc - 1) / tpc);
+        err = launch_pdl(plan_dispatch_tiles_kernel, dim3(blocks), dim3(kThreads), smem, stream,
+                         a, tpc);
+    }
+    if (err != cudaSuccess) {
+        set_cuda_error(err);
+        return MOE_ECUDA;
+    }
+    return check_launch();
+}
+
 } // namespace
 } // namespace moe
 
@@ -246,6 +471,13 @@ MOE_EXPORT int moe_plan_dispatch(const int32_t *topk_idx, const void *x, int64_t
             return MOE_EALIGN;
     }
     const int64_t n = S * (int64_t)K;
+    // larger batches: CTAs own token ranges of at most 1024 entries, one CTA
+    // per SM; each counts all n entries itself, so this stops at kTiledMax
+    const int64_t tpc = (S + sm_count() - 1) / sm_count();
+    if (MOE_PD_TILED && n > kFusedMaxEntries && n <= kTiledMaxEntries && tpc * K <= kThreads)
+        return launch_tiles(topk_idx, x, S, K, E, row_bytes, x_scales, n_scales, cnt, off,
+                            packed_src, tok_map, n_invalid, packed_x, packed_rows, packed_scales,
+                            tpc, (cudaStream_t)stream);
     if (n == 0 || n > kFusedMaxEntries) {
         // throughput path: the two calls it fuses, back to back
         if (int rc = moe_plan(topk_idx, S, K, E, cnt, off, packed_src, tok_map, n_invalid,

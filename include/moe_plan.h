@@ -262,12 +262,14 @@ int moe_dispatch_quant_fp8(const void *x, int64_t S, int64_t H, int K,
  *
  * Computes exactly what moe_plan followed by moe_dispatch computes: the same
  * cnt, off, packed_src, tok_map, n_invalid, packed_x and packed_scales, with
- * the same arguments, layouts and rules as those two calls.  When
- * 0 < S*K <= moe_plan_dispatch_fused_max() one kernel does both (every CTA
- * ranks all entries in shared memory; the workspace is not used); otherwise
- * the call enqueues moe_plan then moe_dispatch, and `workspace` follows
- * moe_plan's rule (moe_plan_workspace_size).  All arguments are checked
- * before anything is enqueued.
+ * the same arguments, layouts and rules as those two calls.  One kernel does
+ * both when 0 < S*K <= moe_plan_dispatch_fused_max() (every CTA ranks all
+ * entries in shared memory) and when S*K <= 131072 with at most 1024 entries
+ * per SM's share of the tokens (each CTA owns a token range: it counts all
+ * entries, ranks its own and copies its own rows); the workspace is then not
+ * used.  Otherwise the call enqueues moe_plan then moe_dispatch, and
+ * `workspace` follows moe_plan's rule (moe_plan_workspace_size).  All
+ * arguments are checked before anything is enqueued.
  * ---------------------------------------------------------------------- */
 int64_t moe_plan_dispatch_fused_max(void);
 int moe_plan_dispatch(const int32_t *topk_idx, const void *x, int64_t S, int64_t H,

@@ -84,6 +84,39 @@ def test_bf16_shapes(S, H, E, K):
     _check(workloads.make("moonep", seed=S + E, S=S, H=H, E=E, K=K))
 
 
+@pytest.mark.parametrize("S,H,E,K", [(4096, 7168, 64, 8), (3000, 264, 1024, 32), (5000, 136, 37, 5),
+                                     (16000, 16, 64, 8), (200, 6144, 256, 8)])
+def test_tiled_one_launch_shapes(S, H, E, K):
+    """Above 1024 entries and up to 131072, one launch whose CTAs own token
+    ranges (the benchmark shape among them); 19456 x 8 would exceed the range."""
+    _check(workloads.make("moonep", seed=S + K, S=S, H=H, E=E, K=K))
+
+
+def test_tiled_with_scales_invalid_and_unaligned_ids():
+    """fp8 rows with scale rows, invalid ids, and a topk_idx that is not
+    16-byte aligned (the counting pass then reads one id at a time)."""
+    import combine_moe_plan_02_gb300 as moe
+    wl = workloads.make("fp8small", seed=11, S=700)
+    idx = wl.topk_idx.copy()
+    idx[::7, 3] = -1
+    idx[5, :] = wl.E
+    _check(wl, idx)
+    wl2 = workloads.make("moonep", seed=12, S=777, H=64, E=16, K=5)
+    big = torch.zeros(wl2.S * wl2.K + 1, dtype=torch.int32, device="cuda")
+    big[1:] = torch.from_numpy(wl2.topk_idx.reshape(-1)).cuda()
+    idx_view = big[1:].view(wl2.S, wl2.K)          # 4-byte aligned only
+    assert idx_view.data_ptr() % 16 != 0
+    x = gpu_path.to_device(wl2)["x"]
+    plan, px, _ = moe.moe_plan_dispatch(idx_view, x, wl2.E)
+    torch.cuda.synchronize()
+    ref = oracle.plan(wl2.topk_idx, wl2.E)
+    assert np.array_equal(np_(plan.tok_map), ref["tok_map"])
+    assert np.array_equal(np_(plan.cnt), ref["cnt"])
+    V = int(ref["off"][-1])
+    assert np.array_equal(np_(px)[:V], oracle.dispatch(wl2.x, ref["tok_map"], V))
+    assert moe.moe_device_errors() == 0
+
+
 def test_invalid_ids_and_repeats():
     wl = workloads.make("fp8small", seed=7, S=100)
     idx = wl.topk_idx.copy()
