@@ -1,4 +1,4 @@
-// Plan and dispatch in one launch for small batches.
+// Plan and dispatch in one launch.
 //
 // Sources: ROCm/mori "EPv2 internode dispatch/combine over CCO/GDA": the
 // page keeps two kernel families, a throughput one and a low-latency one,
@@ -18,6 +18,11 @@
 // the plan outputs.  Then every warp of the grid copies 512-byte segments of
 // token rows (32 lanes x 16 bytes) to the token's destinations, read from
 // the CTA's own copy of the map.  No CTA waits for another CTA.
+//
+// Larger batches (up to kTiledMaxEntries) take plan_dispatch_tiles_kernel,
+// whose CTAs own token ranges instead (see there): a kernel boundary between
+// a separate plan and dispatch costs several microseconds on this part, more
+// than the redundant counting does.
 
 #include "common.cuh"
 
