@@ -115,3 +115,27 @@ def test_plan_replay_with_new_rows():
         ref_out = oracle.combine(ref_packed, "bf16", wl.topk_w, p["tok_map"], wl.H, "bf16")
         assert np.array_equal(gpu_path._np(out), ref_out)
     assert moe.moe_device_errors() == 0
+
+
+def test_quantising_dispatch_into_capacity_buckets():
+    """Quantised rows into the padded buckets of a capacity plan: the kept
+    rows hold the oracle's codes and scales, the rest keep the poison."""
+    import combine_moe_plan_02_gb300 as moe
+    wl = workloads.make("moonep", seed=91, S=400, H=1024, E=16, K=4)
+    cap = 60
+    dev = torch.device("cuda")
+    rows = wl.E * cap
+    out = moe.moe_plan_capacity(torch.from_numpy(wl.topk_idx).to(dev), wl.E, cap)
+    x = torch.from_numpy(wl.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    q = gpu_path.poisoned((rows, wl.H), torch.uint8)
+    sc = gpu_path.poisoned((rows, wl.H // 128), torch.float32)
+    moe.moe_dispatch_quant_fp8(x, out.tok_map, packed_q=q, packed_scales=sc)
+    torch.cuda.synchronize()
+    assert moe.moe_device_errors() == 0
+    ref = oracle.plan_capacity(wl.topk_idx, wl.E, cap)
+    assert ref["n_dropped"] > 0
+    q0, sc0 = oracle.quant_fp8(wl.x, 128)
+    ref_q = oracle.dispatch(q0, ref["tok_map"], rows, fill=gpu_path.POISON)
+    ref_s = oracle.dispatch(sc0, ref["tok_map"], rows, fill=gpu_path.POISON)
+    assert np.array_equal(gpu_path._np(q), ref_q)
+    assert np.array_equal(gpu_path._np(sc).view(np.uint32), ref_s.view(np.uint32))
