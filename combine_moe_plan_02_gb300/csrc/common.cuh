@@ -97,6 +97,10 @@ cudaError_t prepare_kernel(F fn, size_t smem, int threads, KernelCache &kc, int 
     return cudaSuccess;
 }
 
+#ifndef MOE_USE_PDL
+#define MOE_USE_PDL 1
+#endif
+
 // Launch with programmatic dependent launch allowed: the kernel may start
 // while its predecessor in the stream is finishing, and must execute
 // griddep_wait() before touching memory that earlier work reads or writes.
@@ -111,9 +115,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-#ifndef MOE_USE_PDL
-#define MOE_USE_PDL 1
-#endif
     attr[0].val.programmaticStreamSerializationAllowed = MOE_USE_PDL;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -244,6 +245,14 @@ __device__ __forceinline__ uint2 ld_stream8(const void *p)
 __device__ __forceinline__ void st8(void *p, uint2 v)
 {
     asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+// 16-byte store marked streaming (evict first)
+__device__ __forceinline__ void st16_cs(void *p, uint4 v)
+{
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
 }
 
 __device__ __forceinline__ void st16(void *p, uint4 v)
