@@ -729,7 +729,8 @@ def run_ours(args):
                    "S": S, "H": H, "E": E, "K": K, "valid_rows": V,
                    "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write + "
                          f"{L2_FLUSH_BYTES >> 20} MiB read, untimed)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "step": "moe_plan_dispatch (plan + dispatch, one launch) + moe_combine"},
         "per_call": {"plan": percall("plan", t_plan), "dispatch": percall("dispatch", t_disp),
                      "combine": percall("combine", t_comb),
                      "plan_dispatch": percall("plan_dispatch", t_pd,
