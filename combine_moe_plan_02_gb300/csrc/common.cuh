@@ -255,6 +255,13 @@ __device__ __forceinline__ void st16_cs(void *p, uint4 v)
                  : "memory");
 }
 
+// Asks the bulk-copy engine to bring [p, p + bytes) into L2 (no completion
+// to wait for).  p 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void st16(void *p, uint4 v)
 {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),

@@ -238,6 +238,13 @@ __global__ void __launch_bounds__(kThreads, 1) plan_dispatch_kernel(PDArgs a)
 #ifndef MOE_PD_STORE_CS
 #define MOE_PD_STORE_CS 1
 #endif
+#ifndef MOE_PD_PREFETCH
+#define MOE_PD_PREFETCH 1
+#endif
+#ifndef MOE_PD_PREFETCH_CHUNK
+#define MOE_PD_PREFETCH_CHUNK 65536
+#endif
+constexpr int64_t kPrefetchChunk = MOE_PD_PREFETCH_CHUNK;  // bytes per L2 prefetch request
 constexpr int kTilePre = 8;     // 16-byte index groups per thread loaded up front
 constexpr int kCopyUnroll = 4;  // row segments per warp with loads in flight
 
@@ -261,6 +268,23 @@ __global__ void __launch_bounds__(kThreads, 1) plan_dispatch_tiles_kernel(PDArgs
     const int64_t t0 = (int64_t)blockIdx.x * tpc;
     const int64_t t1 = min(t0 + tpc, a.S);
     const int64_t b0 = t0 * a.K, b1 = t1 * a.K;   // own entries [b0, b1)
+
+#if MOE_PD_PREFETCH
+    // The range's token rows (one contiguous span of x, and of the scales)
+    // are pulled into L2 while the CTA plans, when DRAM has little else to
+    // do, so that the copies afterwards mostly hit L2 (plan + dispatch 95.8
+    // -> 93.0 us at the MoonEP shape).  An evict-last priority on these lines,
+    // set back to normal as each is read, measured slower (93.5-95.6 us).
+    {
+        const int64_t hi = (t1 - t0) * a.row_bytes, shi = (t1 - t0) * a.scale_bytes;
+        const uint8_t *xr = a.x + t0 * a.row_bytes;
+        for (int64_t p = (int64_t)threadIdx.x * kPrefetchChunk; p < hi;
+             p += (int64_t)kThreads * kPrefetchChunk)
+            prefetch_l2_bulk(xr + p, (uint32_t)min(kPrefetchChunk, hi - p));
+        if (shi > 0 && threadIdx.x == kThreads - 1)
+            prefetch_l2_bulk(a.xs + t0 * a.scale_bytes, (uint32_t)shi);
+    }
+#endif
 
     // first loads: this warp's own chunk and the first index groups of the
     // all-entries pass, so that their latency overlaps the set-up
