@@ -252,6 +252,86 @@ __global__ void __launch_bounds__(kThreads, MOE_COMBINE_MIN_BLOCKS) combine_kern
 }
 
 // ---------------------------------------------------------------------------
+// The same sum for the common case -- bf16 rows in and out, weights per
+// output row, K <= 8, no weight fold -- written to hold fewer registers so
+// that more warps fit on an SM and more gathers are in flight: per unit the
+// lanes keep one row pointer each (shuffled to the warp when a step issues
+// its loads) and one ballot of the valid entries instead of K row indices,
+// and each 32-bit word of a gathered vector is widened and added in place.
+// The order of operations is the kernel's above.
+// ---------------------------------------------------------------------------
+
+#ifndef MOE_COMBINE_LEAN
+#define MOE_COMBINE_LEAN 1
+#endif
+#ifndef MOE_COMBINE_LEAN_MIN_BLOCKS
+#define MOE_COMBINE_LEAN_MIN_BLOCKS 3
+#endif
+
+__global__ void __launch_bounds__(kThreads, MOE_COMBINE_LEAN_MIN_BLOCKS)
+combine_lean_kernel(CombineArgs a)
+{
+    griddep_wait();  // y, map, weights come from earlier stream work
+    griddep_launch_dependents();
+
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+    const int64_t W = ((int64_t)gridDim.x * kThreads) >> 5;
+    const int64_t units = a.rows * a.slices;
+    const int K = a.K;
+    const int64_t row_bytes = a.steps * 16;  // bf16 rows, in and out
+
+    for (int64_t u = gw; u < units; u += W) {
+        const int64_t i = u / a.slices;
+        const int sl = (int)(u - i * a.slices);
+        const uint8_t *base = a.y;  // this lane's y row (lane k <-> entry k)
+        float w = 0.0f;
+        bool valid = false;
+        if (lane < K) {
+            const int64_t r = __ldg(a.map + i * K + lane);
+            if (r >= 0 && r < a.y_rows) {
+                valid = true;
+                base = a.y + r * row_bytes;
+                w = __ldg(a.w + i * K + lane);
+            } else if (r != -1) {
+                atomicOr(&g_combine_error, kErrCombineIndex);  // dropped, never gathered
+            }
+        }
+        const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+        const int64_t pbase = (int64_t)sl * 32 * a.R;
+        uint8_t *out_row = a.out + i * row_bytes;
+        for (int r = 0; r < a.R; ++r) {
+            const int64_t p = pbase + (int64_t)r * 32 + lane;
+            const bool active = p < a.steps;
+            uint4 v[kKChunk];
+#pragma unroll
+            for (int k = 0; k < kKChunk; ++k) {
+                const uint8_t *bk = reinterpret_cast<const uint8_t *>(
+                    __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(base), k));
+                if (active && ((vmask >> k) & 1u)) v[k] = ld_stream16(bk + p * 16);
+            }
+            float acc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+#pragma unroll
+            for (int k = 0; k < kKChunk; ++k) {
+                const float wk = __shfl_sync(0xffffffffu, w, k);
+                if (active && ((vmask >> k) & 1u)) {
+                    const uint32_t q[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        acc[2 * e] = __fadd_rn(acc[2 * e], __fmul_rn(wk, __uint_as_float(q[e] << 16)));
+                        acc[2 * e + 1] =
+                            __fadd_rn(acc[2 * e + 1], __fmul_rn(wk, __uint_as_float(q[e] & 0xffff0000u)));
+                    }
+                }
+            }
+            if (active) Io<__nv_bfloat16>::store(out_row, p, acc, false);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Dedup combine in one pass (K <= kKChunk).  The work unit is (token s,
 // slice).  Lane k holds the token's group-row entry gtok_map[s,k] (set for the
 // first entry of each group: the representatives, in increasing k) and, after
@@ -424,9 +504,16 @@ int launch_combine(CombineArgs &a, int in_dt, int out_dt, int wm, cudaStream_t s
 {
     void (*fn)(CombineArgs) = select_kernel(in_dt, out_dt, wm);
     if (!fn) return MOE_EINVAL;
-    // one cache per (input, output, weight-mode) kernel
+    // one cache per (input, output, weight-mode) kernel, one for the lean one
     static KernelCache caches[2][2][3];
-    KernelCache &cache = caches[in_dt == MOE_F32][out_dt == MOE_F32][wm];
+    static KernelCache lean_cache;
+    KernelCache *cp = &caches[in_dt == MOE_F32][out_dt == MOE_F32][wm];
+    if (MOE_COMBINE_LEAN && in_dt == MOE_BF16 && out_dt == MOE_BF16 && wm == kWeightDirect &&
+        a.K <= kKChunk && !a.out_w && !a.rows_dev) {
+        fn = combine_lean_kernel;
+        cp = &lean_cache;
+    }
+    KernelCache &cache = *cp;
     int per_sm = 0;
     cudaError_t err = prepare_kernel(fn, 0, kThreads, cache, &per_sm);
     if (err != cudaSuccess || per_sm < 1) {

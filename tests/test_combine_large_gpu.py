@@ -68,3 +68,36 @@ def test_large_combine_matches_oracle(S, H, E, K, out_dt, weighted, holes):
         f"{int((got != ref).sum())} elements differ"
     if holes:
         assert not got[5].view(np.uint8).any()   # +0.0 everywhere
+
+
+@pytest.mark.timeout(300)
+@pytest.mark.parametrize("out_dt", ["bf16", "f32"])
+def test_out_of_range_map_entries_are_dropped_and_reported(out_dt):
+    """Map entries outside [-1, y_rows) are never gathered: the term is
+    dropped, bit 2 of the device error word is set, and every other term is
+    summed as usual (bf16 output takes the K <= 8 bf16 kernel, f32 output the
+    general one)."""
+    import combine_moe_plan_02_gb300 as moe
+    S, H, E, K = 600, 1032, 32, 8
+    wl, idx, p, y = _inputs(S, H, E, K, seed=77, holes=False)
+    V = y.shape[0]
+    bad = p["tok_map"].copy()
+    bad[3, 2] = V                 # one past the end of y
+    bad[10, 0] = V + 12345
+    bad[11, 7] = 1 << 40
+    bad[20, 4] = -7
+    dropped = bad.copy()
+    dropped[(dropped >= V) | (dropped < -1)] = -1
+    assert moe.moe_device_errors() == 0
+    dev = torch.device("cuda")
+    yd = torch.from_numpy(y.view(np.int16)).to(dev).view(torch.bfloat16)
+    tdt = torch.float32 if out_dt == "f32" else torch.bfloat16
+    out = gpu_path.poisoned((S, H), tdt)
+    moe.moe_combine(yd, torch.from_numpy(wl.topk_w).to(dev), torch.from_numpy(bad).to(dev),
+                    out=out)
+    torch.cuda.synchronize()
+    assert moe.moe_device_errors() & 4
+    got = out.cpu()
+    got = got.view(torch.int16).numpy().view(np.uint16) if out_dt == "bf16" else got.numpy()
+    ref = oracle.combine(y, "bf16", wl.topk_w, dropped, H, out_dt)
+    assert np.array_equal(got.view(np.uint8), ref.view(np.uint8))
