@@ -310,7 +310,8 @@ int moe_dispatch_dedup(const void *x, int64_t S, int64_t H, int dtype, int K, in
  * separately (no fused multiply-add); bf16 output rounds to nearest even.
  *
  * y       [y_rows, H] of in_dtype (MOE_BF16 or MOE_F32), 1 <= y_rows < 2^31;
- *         a map entry at or past y_rows drops its term and is flagged (bit 2)
+ *         a map entry at or past y_rows, or below -1, drops its term and is
+ *         flagged (bit 2)
  * topk_w  f32 [S, K]; tok_map int64 [S, K] from moe_plan
  * out     [S, H] of out_dtype (MOE_BF16 or MOE_F32)
  * Alignment: y, out 16-byte aligned; H a multiple of 8.
