@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) dispatch_bulk_kernel(CopyAr
         for (int st = 0; st < kStages; ++st) {
             const int64_t j = j0 + st;
             if (j >= n_mine || !ok) break;
-            // every lane that stores waits on the barrier itself; the verdict
+            // every lane that stores waits on the barrier itself; the outcome
             // is made warp-uniform so the warp never splits around __syncwarp
             const bool landed = mbar_wait_bounded(&bar[st], (uint32_t)((j / kStages) & 1));
             if (!__all_sync(0xffffffffu, landed)) {
