@@ -35,6 +35,7 @@ import workloads  # noqa: E402
 METRIC = "dispatch & combine GB/s and % HBM roofline at S=4096 H=7168 E=64 K=8; µs/call"
 WORKLOAD = "moonep"
 FALLBACK_HBM_GBS = 6800.0
+SPEC_HBM_GBS = 8000.0     # GB300 HBM3e, nominal (~8 TB/s)
 L2_FLUSH_BYTES = 512 << 20
 
 
@@ -221,16 +222,158 @@ def barrier(world: int, device=None):
 ORACLE_SAMPLE_TOKENS = 1024
 
 
-def oracle_sample(seed: int = 0):
-    """A bounded sample of the workload: the first 1024 tokens of the batch,
-    with the expert output rows prepared once."""
-    import oracle
-    wl = workloads.make(WORKLOAD, seed=seed)
-    n = ORACLE_SAMPLE_TOKENS
+def host_cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the
+    machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+class PinnedCore:
+    """Pins the calling thread (where the oracle runs) to one logical CPU,
+    the highest-numbered one it may use, and restores the old set on exit."""
+
+    def __enter__(self):
+        self.old = os.sched_getaffinity(0)
+        self.core = max(self.old)
+        os.sched_setaffinity(0, {self.core})
+        try:
+            with open(f"/sys/devices/system/cpu/cpu{self.core}/topology/thread_siblings_list") as f:
+                self.siblings = f.read().strip()
+        except Exception:
+            self.siblings = None
+        return self
+
+    def __exit__(self, *exc):
+        os.sched_setaffinity(0, self.old)
+        return False
+
+
+def _median_us(fn, reps: int = 3):
+    """Median µs of `reps` calls after one untimed warm-up call."""
+    fn()
+    ts = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        fn()
+        ts.append(time.perf_counter() - t0)
+    return 1e6 * statistics.median(ts)
+
+
+def _head(wl, n):
+    """The first n tokens of a workload (a bounded sample of the batch)."""
     wl.S = n
     wl.topk_idx = np.ascontiguousarray(wl.topk_idx[:n])
     wl.topk_w = np.ascontiguousarray(wl.topk_w[:n])
     wl.x = np.ascontiguousarray(wl.x[:n])
+    if wl.x_scales is not None:
+        wl.x_scales = np.ascontiguousarray(wl.x_scales[:n])
+    return wl
+
+
+def _oracle_calls(wl):
+    """Oracle calls of one workload, inputs prepared once (the expert output
+    rows y of the harness's expert stage included, untimed): name ->
+    (callable, algorithmic bytes)."""
+    import oracle
+    S, H, E, K = wl.S, wl.H, wl.E, wl.K
+    p = oracle.plan(wl.topk_idx, wl.E)
+    V = int(p["off"][-1])
+    tm = p["tok_map"]
+    calls = {}
+    if wl.dtype == workloads.DT_FP8:
+        nsc = wl.x_scales.shape[1]
+        packed = oracle.dispatch(wl.x, tm, V)
+        pscales = oracle.dispatch(wl.x_scales, tm, V)
+        y = oracle.expert_dequant_fp8(packed, pscales, wl.scale_block)
+        calls["plan"] = (lambda: oracle.plan(wl.topk_idx, E), algorithmic_bytes(S, H, E, K, V)["plan"])
+        calls["dispatch"] = (lambda: (oracle.dispatch(wl.x, tm, V), oracle.dispatch(wl.x_scales, tm, V)),
+                             S * H + S * K * 8 + V * H + (S + V) * nsc * 4)
+        calls["combine"] = (lambda: oracle.combine(y, "bf16", wl.topk_w, tm, H, "bf16"),
+                            algorithmic_bytes(S, H, E, K, V)["combine"])
+        return calls
+    b = 2 if wl.dtype == workloads.DT_BF16 else 4
+    dt = "bf16" if wl.dtype == workloads.DT_BF16 else "f32"
+    nby = algorithmic_bytes(S, H, E, K, V, elem=b, out_elem=b)
+    packed = oracle.dispatch(wl.x, tm, V)
+    if wl.dtype == workloads.DT_BF16:
+        y = oracle.expert_scale_bf16(packed, p["off"], wl.expert_scale)
+    else:
+        y = packed                                   # identity experts
+    calls["plan"] = (lambda: oracle.plan(wl.topk_idx, E), nby["plan"])
+    calls["dispatch"] = (lambda: oracle.dispatch(wl.x, tm, V), nby["dispatch"])
+    calls["combine"] = (lambda: oracle.combine(y, dt, wl.topk_w, tm, H, dt), nby["combine"])
+    if wl.group_size:
+        gs = wl.group_size
+        gp = oracle.group_plan(wl.topk_idx, tm, E, gs)
+        R = int(gp["goff"][-1])
+        calls["group_plan"] = (lambda: oracle.group_plan(wl.topk_idx, tm, E, gs),
+                               S * K * (4 + 8) + S * K * 8 + R * (4 + 8 * K) + (E // gs) * 12)
+        calls["dispatch_dedup"] = (
+            lambda: oracle.dispatch_dedup(wl.x, gp["grp_src"], gp["grp_tok_map"], K, V),
+            S * H * b + R * H * b + V * H * b + R * (4 + 8 * K))
+        calls["combine_dedup"] = (
+            lambda: oracle.combine_dedup(y, dt, wl.topk_w, gp["grp_src"], gp["grp_tok_map"],
+                                         gp["gtok_map"], H, dt),
+            V * H * b + R * H * b + S * H * b + R * 8 * K + S * K * 16)
+    return calls
+
+
+def _time_calls(calls):
+    res = {}
+    for name, (fn, nbytes) in calls.items():
+        us = _median_us(fn)
+        res[name] = {"us": round(us, 1), "GB_per_s": round(nbytes / (us * 1e-6) / 1e9, 3),
+                     "algorithmic_bytes": int(nbytes)}
+    return res
+
+
+def cpu_per_config():
+    """µs per oracle call and GB/s for each of the five workloads: the tiny
+    case, the dedup shape (with S=0 and S=1) and the small-token fp8 sweep
+    at full size; the MoonEP and Zipf shapes on their first 1024 tokens."""
+    per = {}
+    per["tiny"] = {"sample": "full: S=128 H=256 E=8 K=2 bf16",
+                   "calls": _time_calls(_oracle_calls(workloads.make("tiny", seed=0)))}
+    for name in ("moonep", "zipf"):
+        wl = workloads.make(name, seed=0)
+        full = wl.S
+        wl = _head(wl, ORACLE_SAMPLE_TOKENS)
+        per[name] = {"sample": f"first {ORACLE_SAMPLE_TOKENS} of {full} tokens "
+                               f"(H={wl.H} E={wl.E} K={wl.K} bf16)",
+                     "calls": _time_calls(_oracle_calls(wl))}
+    ded = {}
+    for S in (4096, 0, 1):
+        ded[f"S={S}"] = _time_calls(_oracle_calls(workloads.make("dedup", seed=0, S=S)))
+    per["dedup"] = {"sample": "full: S=4096 H=4096 E=64 in 8 groups, K=8 f32; and S=0, S=1",
+                    "calls": ded}
+    fp8 = {}
+    for S in workloads.FP8_SWEEP_TOKENS:
+        fp8[f"S={S}"] = _time_calls(_oracle_calls(workloads.make("fp8small", seed=S, S=S)))
+    per["fp8small"] = {"sample": "full: S in {4,8,16,32,128,1024}, H=6144 E=256 K=8, fp8 rows "
+                                 "+ f32 scales, bf16 combine", "calls": fp8}
+    return per
+
+
+def oracle_sample(seed: int = 0):
+    """A bounded sample of the workload: the first 1024 tokens of the batch,
+    with the expert output rows prepared once."""
+    import oracle
+    wl = _head(workloads.make(WORKLOAD, seed=seed), ORACLE_SAMPLE_TOKENS)
     p = oracle.plan(wl.topk_idx, wl.E)
     V = int(p["off"][-1])
     packed = oracle.dispatch(wl.x, p["tok_map"], V)
@@ -245,37 +388,39 @@ def oracle_step(wl, y, V):
     oracle.combine(y, "bf16", wl.topk_w, p["tok_map"], wl.H, "bf16")
 
 
-def cpu_baseline(min_seconds: float = 10.0, max_passes: int = 200):
-    wl, y, V = oracle_sample()
-    by = sum(algorithmic_bytes(wl.S, wl.H, wl.E, wl.K, V).values())
-    oracle_step(wl, y, V)  # warm
-    t0 = time.perf_counter()
-    n = 0
-    while n < max_passes:
-        oracle_step(wl, y, V)
-        n += 1
-        if time.perf_counter() - t0 >= min_seconds:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": by * n / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+def cpu_baseline():
+    """The single-threaded C oracle on one pinned core: `value` is
+    plan + dispatch + combine on the first 1024 tokens of the MoonEP batch
+    (algorithmic bytes / summed median call times); `per_config` has every
+    workload."""
+    with PinnedCore() as pin:
+        per = cpu_per_config()
+    calls = per[WORKLOAD]["calls"]
+    by = sum(c["algorithmic_bytes"] for c in calls.values())
+    us = sum(c["us"] for c in calls.values())
+    return {"value": by / (us * 1e-6) / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"first {ORACLE_SAMPLE_TOKENS} of the 4096 tokens (H=7168 E=64 K=8 bf16), "
-                      f"plan+dispatch+combine, {n} passes in {dt:.1f} s, single-threaded C oracle",
-            "seconds": round(dt, 2)}
+                      "plan+dispatch+combine, median of 3 timed calls each after a warm-up, "
+                      "single-threaded C oracle",
+            "pinned_core": pin.core, "core_siblings": pin.siblings,
+            "cpu_model": host_cpu_model(), "host_cpus": os.cpu_count(), "per_config": per}
 
 
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    wl, y, V = oracle_sample()
-    by = sum(algorithmic_bytes(wl.S, wl.H, wl.E, wl.K, V).values())
-    for _ in range(args.warmup):
-        oracle_step(wl, y, V)
-    times = []
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        oracle_step(wl, y, V)
-        times.append(time.perf_counter() - t0)
+    with PinnedCore() as pin:
+        wl, y, V = oracle_sample()
+        by = sum(algorithmic_bytes(wl.S, wl.H, wl.E, wl.K, V).values())
+        for _ in range(args.warmup):
+            oracle_step(wl, y, V)
+        times = []
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            oracle_step(wl, y, V)
+            times.append(time.perf_counter() - t0)
+        per = cpu_per_config()
     ms = 1e3 * sum(times) / len(times)
     value = by / (ms / 1e3) / 1e9
     line = {
@@ -286,7 +431,10 @@ def run_reference(args):
                                "H=7168 E=64 K=8 bf16 per step (CPU oracle)",
                    "S": ORACLE_SAMPLE_TOKENS, "H": wl.H, "E": wl.E, "K": wl.K},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"first {ORACLE_SAMPLE_TOKENS} tokens per step"},
+                         "sample": f"first {ORACLE_SAMPLE_TOKENS} tokens per step",
+                         "pinned_core": pin.core, "core_siblings": pin.siblings,
+                         "cpu_model": host_cpu_model(), "host_cpus": os.cpu_count(),
+                         "per_config": per},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -722,7 +870,8 @@ def run_ours(args):
         gbs = nb / (m / 1e3) / 1e9
         return {"us": round(1e3 * m, 2), "us_median": round(1e3 * statistics.median(ts), 2),
                 "us_min": round(1e3 * min(ts), 2), "GB_per_s": round(gbs, 1),
-                "frac_of_peak": round(gbs / peak, 4), "algorithmic_bytes": nb}
+                "frac_of_peak": round(gbs / peak, 4), "frac_of_spec": round(gbs / SPEC_HBM_GBS, 4),
+                "algorithmic_bytes": nb}
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": n,
@@ -746,6 +895,8 @@ def run_ours(args):
                      "algorithmic_bytes": dom_bytes, "us": round(1e3 * dom_ms, 2),
                      "peak": peak, "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "spec_peak": SPEC_HBM_GBS,
+                     "frac_of_spec": round(achieved / SPEC_HBM_GBS, 4),
                      "traffic": kernel_traffic(dom)},
         "e2e": {"value": e2e_pipe_bytes / (e2e_pipe_ms / 1e3) / 1e9, "unit": "GB/s",
                 "ms_per_step": e2e_pipe_ms / n,
@@ -786,15 +937,38 @@ def run_ours(args):
         line["dispatch_quant_fp8"] = {
             "us": round(1e3 * tq, 2), "GB_per_s": round(qbytes / (tq / 1e3) / 1e9, 1),
             "frac_of_peak": round(qbytes / (tq / 1e3) / 1e9 / peak, 4),
+            "frac_of_spec": round(qbytes / (tq / 1e3) / 1e9 / SPEC_HBM_GBS, 4),
             "algorithmic_bytes": qbytes, "traffic": kernel_traffic("dispatch_quant_fp8"),
             "what": "bf16 rows -> E4M3 codes + f32 scale per 128 elements, K packed rows each"}
+        del pq, psc
+        # the weight fold (unweighted, with out_weights) and the capacity plan
+        # on the same batch, each timed alone with L2 flushed before it
+        ow = torch.empty(S, K, dtype=torch.float32, device=dev)
+        cap = (S * K // E) * 5 // 4                  # 1.25 x the mean load per expert
+        cplan = moe.moe_plan_capacity(idx, E, cap)
+        tx = _timed_calls(torch, stream, flush_l2, {
+            "combine_fold": lambda: moe.moe_combine_fold(y, w, plan.tok_map, weighted=False,
+                                                         out=out, out_weights=ow, stream=stream),
+            "plan_capacity": lambda: moe.moe_plan_capacity(idx, E, cap, out=cplan, workspace=ws,
+                                                           stream=stream)}, n=n)
+        kept = S * K - int(cplan.n_dropped.item())
+        xb = {"combine_fold": V * H * 2 + S * K * (8 + 4 + 4) + S * H * 2,
+              "plan_capacity": S * K * 4 + E * 4 + (E + 1) * 8 + kept * 4 + S * K * 8 + 8}
+        for k_, us_ in tx.items():
+            gbs = xb[k_] / (us_ * 1e-6) / 1e9
+            line["per_call"][k_] = {"us": round(us_, 2), "GB_per_s": round(gbs, 1),
+                                    "frac_of_peak": round(gbs / peak, 4),
+                                    "frac_of_spec": round(gbs / SPEC_HBM_GBS, 4),
+                                    "algorithmic_bytes": xb[k_]}
+        line["per_call"]["combine_fold"]["what"] = "unweighted, with out_weights (weight fold)"
+        line["per_call"]["plan_capacity"]["what"] = (f"capacity {cap} rows per expert "
+                                                     f"(1.25 x mean load), {S * K - kept} dropped")
     if rank == 0 and not args.no_small_tokens:
         line["small_tokens"] = small_token_latency(dev)
     if rank == 0 and not args.no_other_workloads:
         line["other_workloads"] = other_workloads(torch, moe, dev, stream, flush_l2, peak)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
-        line["cpu_baseline"]["host_cpus"] = os.cpu_count()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

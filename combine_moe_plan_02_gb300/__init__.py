@@ -279,7 +279,8 @@ def moe_dispatch_dedup(x: torch.Tensor, gp: GroupPlan, *, packed_x: Optional[tor
         packed_x = torch.empty(S * K, H, dtype=x.dtype, device=x.device)
     _abi.check("moe_dispatch_dedup", lib().moe_dispatch_dedup(
         _ptr(x), S, H, _dt(x), K, gp.G, _ptr(gp.goff), _ptr(gp.grp_src), _ptr(gp.grp_tok_map),
-        _ptr(gp.gtok_map), gp.max_rows, _ptr(grp_x), _ptr(packed_x), _stream(stream)))
+        _ptr(gp.gtok_map), gp.max_rows, _ptr(grp_x), _ptr(packed_x), packed_x.shape[0],
+        _stream(stream)))
     return grp_x, packed_x
 
 
@@ -309,7 +310,7 @@ def moe_combine_dedup(y: torch.Tensor, topk_w: torch.Tensor, gp: GroupPlan, *,
     if out is None:
         out = torch.empty(S, H, dtype=out_dtype, device=y.device)
     _abi.check("moe_combine_dedup", lib().moe_combine_dedup(
-        _ptr(y), _dt(y), _ptr(topk_w), _ptr(gp.goff), gp.G, _ptr(gp.grp_src),
+        _ptr(y), y.shape[0], _dt(y), _ptr(topk_w), _ptr(gp.goff), gp.G, _ptr(gp.grp_src),
         _ptr(gp.grp_tok_map), _ptr(gp.gtok_map), S, H, K, gp.max_rows, _ptr(gtok), _ptr(out),
         _dt(out), _stream(stream)))
     return gtok, out

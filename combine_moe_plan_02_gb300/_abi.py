@@ -10,7 +10,9 @@ import os
 import re
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "libmoe_gb300.so")
+# MOE_GB300_LIB names another build of the same library (e.g. one compiled
+# with different options); by default the in-tree build is loaded.
+LIB_PATH = os.environ.get("MOE_GB300_LIB") or os.path.join(PKG, "libmoe_gb300.so")
 HEADER = os.path.join(os.path.dirname(PKG), "include", "moe_plan.h")
 
 MOE_OK, MOE_EINVAL, MOE_EALIGN, MOE_ECUDA = 0, 1, 2, 3
@@ -30,10 +32,11 @@ SIGNATURES = {
     "moe_group_plan_workspace_size": (SZ, [I64, I32, I32, I32]),
     "moe_group_plan": (I32, [P, P, I64, I32, I32, I32, P, P, P, P, P, P, SZ, P]),
     "moe_dispatch": (I32, [P, I64, I64, I32, I32, P, P, I64, P, I64, P, P]),
-    "moe_dispatch_dedup": (I32, [P, I64, I64, I32, I32, I32, P, P, P, P, I64, P, P, P]),
+    "moe_dispatch_dedup": (I32, [P, I64, I64, I32, I32, I32, P, P, P, P, I64, P, P, I64, P]),
     "moe_dispatch_quant_fp8": (I32, [P, I64, I64, I32, P, I32, P, P, I64, P]),
     "moe_combine": (I32, [P, I64, I32, P, P, I64, I64, I32, P, I32, P]),
-    "moe_combine_dedup": (I32, [P, I32, P, P, I32, P, P, P, I64, I64, I32, I64, P, P, I32, P]),
+    "moe_combine_dedup": (I32, [P, I64, I32, P, P, I32, P, P, P, I64, I64, I32, I64, P, P, I32,
+                                P]),
     "moe_combine_fold": (I32, [P, I64, I32, P, I32, P, I64, I64, I32, P, I32, P, P]),
     "moe_plan_dispatch_fused_max": (I64, []),
     "moe_plan_dispatch": (I32, [P, P, I64, I64, I32, I32, I32, P, I64, P, P, P, P, P, P, I64, P,

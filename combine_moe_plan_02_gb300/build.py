@@ -38,18 +38,23 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, out: str = LIB, build_dir: str = BUILD,
+          defines=()) -> str:
+    """Compiles the library into `out` (objects under `build_dir`).  `defines`
+    are extra preprocessor definitions, e.g. ("MOE_USE_PDL=0",) for a build
+    whose launches never overlap their predecessor."""
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     headers = [os.path.join(CSRC, h) for h in HEADERS]
+    flags = NVCC_FLAGS + [f"-D{d}" for d in defines]
     jobs = []
     objs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s] + headers):
-            jobs.append([nvcc, *NVCC_FLAGS, "-c", s, "-o", o])
+            jobs.append([nvcc, *flags, "-c", s, "-o", o])
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -61,9 +66,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=max(1, len(jobs))) as ex:
         list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB, objs):
-        run([nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", LIB, *objs])
-    return LIB
+    if force or jobs or _stale(out, objs):
+        run([nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", out, *objs])
+    return out
 
 
 if __name__ == "__main__":

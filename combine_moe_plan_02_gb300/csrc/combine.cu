@@ -582,6 +582,7 @@ MOE_EXPORT int moe_combine(const void *y, int64_t y_rows, int in_dtype, const fl
                            const int64_t *tok_map, int64_t S, int64_t H, int K, void *out,
                            int out_dtype, moe_stream_t stream)
 {
+    MOE_TRACE("moe_combine");
     if (!combine_dtype_ok(in_dtype) || !combine_dtype_ok(out_dtype)) return MOE_EINVAL;
     if (S < 0 || H < 1 || K < 1 || K > 32) return MOE_EINVAL;
     if (S == 0) return MOE_OK;
@@ -601,23 +602,26 @@ MOE_EXPORT int moe_combine(const void *y, int64_t y_rows, int in_dtype, const fl
     return launch_combine(a, in_dtype, out_dtype, kWeightDirect, (cudaStream_t)stream);
 }
 
-MOE_EXPORT int moe_combine_dedup(const void *y, int in_dtype, const float *topk_w,
-                                 const int64_t *goff, int G, const int32_t *grp_src,
-                                 const int64_t *grp_tok_map, const int64_t *gtok_map, int64_t S,
-                                 int64_t H, int K, int64_t max_rows, float *gtok, void *out,
-                                 int out_dtype, moe_stream_t stream)
+MOE_EXPORT int moe_combine_dedup(const void *y, int64_t y_rows, int in_dtype,
+                                 const float *topk_w, const int64_t *goff, int G,
+                                 const int32_t *grp_src, const int64_t *grp_tok_map,
+                                 const int64_t *gtok_map, int64_t S, int64_t H, int K,
+                                 int64_t max_rows, float *gtok, void *out, int out_dtype,
+                                 moe_stream_t stream)
 {
+    MOE_TRACE("moe_combine_dedup");
     if (!combine_dtype_ok(in_dtype) || !combine_dtype_ok(out_dtype)) return MOE_EINVAL;
     if (S < 0 || H < 1 || K < 1 || K > 32 || G < 1 || G > 1024) return MOE_EINVAL;
     if (S == 0) return MOE_OK;
-    if (!y || !topk_w || !goff || !grp_src || !grp_tok_map || !gtok_map || !gtok || !out)
+    if (!y || !topk_w || !goff || !grp_src || !grp_tok_map || !gtok_map || !gtok || !out ||
+        y_rows < 1 || y_rows >= ((int64_t)1 << 31))
         return MOE_EINVAL;
     if (max_rows < S * (int64_t)(K < G ? K : G)) return MOE_EINVAL;
     if (H % 8 || !aligned16(y) || !aligned16(out) || !aligned16(gtok)) return MOE_EALIGN;
     if (K <= kKChunk) {
         DedupArgs d = {};
         d.y = static_cast<const uint8_t *>(y);
-        d.y_rows = S * (int64_t)K;
+        d.y_rows = y_rows;
         d.w = topk_w;
         d.gtok_map = gtok_map;
         d.grp_tok_map = grp_tok_map;
@@ -638,7 +642,7 @@ MOE_EXPORT int moe_combine_dedup(const void *y, int in_dtype, const float *topk_
     a.map = grp_tok_map;
     a.rows = max_rows;
     a.rows_dev = goff + G;
-    a.y_rows = S * (int64_t)K;
+    a.y_rows = y_rows;
     a.w_rows = S;
     a.K = K;
     a.H = H;
@@ -664,6 +668,7 @@ MOE_EXPORT int moe_combine_fold(const void *y, int64_t y_rows, int in_dtype,
                                 int64_t H, int K, void *out, int out_dtype, float *out_weights,
                                 moe_stream_t stream)
 {
+    MOE_TRACE("moe_combine_fold");
     if (!combine_dtype_ok(in_dtype) || !combine_dtype_ok(out_dtype)) return MOE_EINVAL;
     if (S < 0 || H < 1 || K < 1 || K > 32 || (weighted != 0 && weighted != 1)) return MOE_EINVAL;
     if (S == 0) return MOE_OK;

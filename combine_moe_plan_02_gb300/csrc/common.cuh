@@ -6,6 +6,13 @@
 
 #include "../../include/moe_plan.h"
 
+#ifndef MOE_NVTX
+#define MOE_NVTX 1
+#endif
+#if MOE_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
+
 #define MOE_EXPORT extern "C" __attribute__((visibility("default")))
 
 namespace moe {
@@ -16,6 +23,30 @@ namespace moe {
 
 // Remembers the CUDA error behind the last MOE_ECUDA on this host thread.
 void set_cuda_error(cudaError_t e);
+
+// A host-side NVTX range around one ABI call, named after the call, so that
+// profilers can attribute the kernels it enqueues (nsys timelines, ncu
+// --nvtx filters).  Header-only NVTX: without a tool attached, a push and a
+// pop cost a few nanoseconds and load nothing.
+struct TraceRange {
+    explicit TraceRange(const char *name)
+    {
+#if MOE_NVTX
+        nvtxRangePushA(name);
+#else
+        (void)name;
+#endif
+    }
+    ~TraceRange()
+    {
+#if MOE_NVTX
+        nvtxRangePop();
+#endif
+    }
+    TraceRange(const TraceRange &) = delete;
+    TraceRange &operator=(const TraceRange &) = delete;
+};
+#define MOE_TRACE(name) ::moe::TraceRange moe_trace_range_(name)
 
 // Returns MOE_ECUDA (recording the error) if the last launch failed.
 inline int check_launch()

@@ -645,6 +645,7 @@ MOE_EXPORT int moe_dispatch(const void *x, int64_t S, int64_t H, int dtype, int 
                             const float *x_scales, int64_t n_scales, float *packed_scales,
                             moe_stream_t stream)
 {
+    MOE_TRACE("moe_dispatch");
     const int es = elem_size(dtype);
     if (es == 0 || S < 0 || H < 1 || K < 1 || K > 32 || n_scales < 0) return MOE_EINVAL;
     if (S == 0) return MOE_OK;
@@ -676,12 +677,14 @@ MOE_EXPORT int moe_dispatch_dedup(const void *x, int64_t S, int64_t H, int dtype
                                   const int64_t *goff, const int32_t *grp_src,
                                   const int64_t *grp_tok_map, const int64_t *gtok_map,
                                   int64_t max_rows, void *grp_x, void *packed_x,
-                                  moe_stream_t stream)
+                                  int64_t packed_rows, moe_stream_t stream)
 {
+    MOE_TRACE("moe_dispatch_dedup");
     const int es = elem_size(dtype);
     if (es == 0 || S < 0 || H < 1 || K < 1 || K > 32 || G < 1 || G > 1024) return MOE_EINVAL;
     if (S == 0) return MOE_OK;
-    if (!x || !goff || !grp_src || !grp_tok_map || !gtok_map || !grp_x || !packed_x)
+    if (!x || !goff || !grp_src || !grp_tok_map || !gtok_map || !grp_x || !packed_x ||
+        packed_rows < 1)
         return MOE_EINVAL;
     if (max_rows < S * (int64_t)(K < G ? K : G)) return MOE_EINVAL;
     const int64_t row_bytes = H * es;
@@ -699,7 +702,7 @@ MOE_EXPORT int moe_dispatch_dedup(const void *x, int64_t S, int64_t H, int dtype
         a.src_div = 1;
         a.dst = static_cast<uint8_t *>(packed_x);
         a.K = K;
-        a.dst_rows = S * (int64_t)K;
+        a.dst_rows = packed_rows;
         a.dst2 = static_cast<uint8_t *>(grp_x);
         a.dst2_rows = max_rows;
         a.gtok_map = gtok_map;
@@ -718,7 +721,7 @@ MOE_EXPORT int moe_dispatch_dedup(const void *x, int64_t S, int64_t H, int dtype
         a.dst = static_cast<uint8_t *>(packed_x);
         a.dst_map = grp_tok_map;
         a.K = K;
-        a.dst_rows = S * (int64_t)K;
+        a.dst_rows = packed_rows;
         a.dst2 = static_cast<uint8_t *>(grp_x);
         a.dst2_rows = max_rows;
         return launch_copy(a, (cudaStream_t)stream);
@@ -741,7 +744,7 @@ MOE_EXPORT int moe_dispatch_dedup(const void *x, int64_t S, int64_t H, int dtype
     a.src_map = nullptr;
     a.src_div = 1;
     a.src_rows = max_rows;
-    a.dst_rows = S * (int64_t)K;
+    a.dst_rows = packed_rows;
     return launch_copy(a, (cudaStream_t)stream);
 }
 
@@ -802,6 +805,7 @@ MOE_EXPORT int moe_dispatch_quant_fp8(const void *x, int64_t S, int64_t H, int K
                                       float *packed_scales, int64_t packed_rows,
                                       moe_stream_t stream)
 {
+    MOE_TRACE("moe_dispatch_quant_fp8");
     if (S < 0 || H < 1 || K < 1 || K > 32) return MOE_EINVAL;
     if (block != 16 && block != 32 && block != 64 && block != 128 && block != 256)
         return MOE_EINVAL;
@@ -858,6 +862,7 @@ MOE_EXPORT int moe_dispatch_quant_fp8(const void *x, int64_t S, int64_t H, int K
 
 MOE_EXPORT int moe_selftest_wait_timeout(int64_t limit_ns, moe_stream_t stream)
 {
+    MOE_TRACE("moe_selftest_wait_timeout");
     if (limit_ns < 1000 || limit_ns > 100000000) return MOE_EINVAL;  // 1 us .. 100 ms
     wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((uint64_t)limit_ns);
     return check_launch();

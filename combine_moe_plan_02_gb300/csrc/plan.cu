@@ -635,6 +635,13 @@ int run_plan(Key key, int nkeys, const PlanGeom &g, const RankOut &o, void *ws,
             set_cuda_error(e);
             return MOE_ECUDA;
         }
+        // A plain launch, not a programmatic dependent one: it starts only
+        // after everything before it on the stream has finished, including
+        // the rank kernel of an earlier plan that may still be reading the
+        // same workspace.  moe_plan_static_scratch depends on this: all its
+        // calls share one array, and a launch_pdl here would let this kernel
+        // overwrite the histograms of the previous call while its rank
+        // kernel (which allows dependents at entry) still reads them.
         plan_hist_kernel<Key><<<g.T, kThreads, smem1, stream>>>(key, nkeys, g,
                                                                  static_cast<int32_t *>(ws));
         if (int rc = check_launch()) return rc;
@@ -676,6 +683,7 @@ MOE_EXPORT int moe_plan(const int32_t *topk_idx, int64_t S, int K, int E, int32_
                         int32_t *n_invalid, void *workspace, size_t workspace_bytes,
                         moe_stream_t stream)
 {
+    MOE_TRACE("moe_plan");
     if (int rc = check_plan_args(S, K, E)) return rc;
     if (!cnt || !off || !n_invalid) return MOE_EINVAL;
     if (S > 0 && (!topk_idx || !packed_src || !tok_map)) return MOE_EINVAL;
@@ -691,6 +699,7 @@ MOE_EXPORT int moe_plan_capacity(const int32_t *topk_idx, int64_t S, int K, int 
                                  int32_t *n_dropped, void *workspace, size_t workspace_bytes,
                                  moe_stream_t stream)
 {
+    MOE_TRACE("moe_plan_capacity");
     if (int rc = check_plan_args(S, K, E)) return rc;
     if (capacity < 1 || capacity * (int64_t)E >= ((int64_t)1 << 31)) return MOE_EINVAL;
     if (!cnt || !off || !n_invalid || !n_dropped) return MOE_EINVAL;
@@ -713,6 +722,7 @@ MOE_EXPORT int moe_group_plan(const int32_t *topk_idx, const int64_t *tok_map, i
                               int64_t *gtok_map, int32_t *grp_src, int64_t *grp_tok_map,
                               void *workspace, size_t workspace_bytes, moe_stream_t stream)
 {
+    MOE_TRACE("moe_group_plan");
     if (int rc = check_plan_args(S, K, E)) return rc;
     if (group_size < 1 || E % group_size) return MOE_EINVAL;
     if (!gcnt || !goff) return MOE_EINVAL;
@@ -761,6 +771,9 @@ void *g_static_scratch_ptr[kMaxStaticDevices];  // device address per device, on
 // Device address of the array on the current device.  In host code the
 // array's name is only a host-side stand-in; the real address comes from
 // cudaGetSymbolAddress, looked up once per device with that device current.
+// The address stays valid for the life of the device's primary context; a
+// cudaDeviceReset after the first call would leave a stale address behind,
+// so resetting a device this library has planned on is not supported.
 int static_scratch_address(void **out)
 {
     int dev = 0;
@@ -792,6 +805,7 @@ MOE_EXPORT int moe_plan_static_scratch(const int32_t *topk_idx, int64_t S, int K
                                        int64_t *tok_map, int32_t *n_invalid,
                                        moe_stream_t stream)
 {
+    MOE_TRACE("moe_plan_static_scratch");
     if (int rc = check_plan_args(S, K, E)) return rc;
     if (!cnt || !off || !n_invalid) return MOE_EINVAL;
     if (S > 0 && (!topk_idx || !packed_src || !tok_map)) return MOE_EINVAL;

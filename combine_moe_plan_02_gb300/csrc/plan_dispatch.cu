@@ -494,6 +494,7 @@ MOE_EXPORT int moe_plan_dispatch(const int32_t *topk_idx, const void *x, int64_t
                                  void *packed_x, int64_t packed_rows, float *packed_scales,
                                  void *workspace, size_t workspace_bytes, moe_stream_t stream)
 {
+    MOE_TRACE("moe_plan_dispatch");
     const int es = elem_size(dtype);
     if (es == 0 || S < 0 || H < 1 || K < 1 || K > 32 || E < 1 || E > 1024 || n_scales < 0 ||
         n_scales > 256)

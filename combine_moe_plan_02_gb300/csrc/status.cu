@@ -32,7 +32,7 @@ int sm_count()
 
 } // namespace moe
 
-MOE_EXPORT int moe_version(void) { return 1; }
+MOE_EXPORT int moe_version(void) { return 2; }
 
 MOE_EXPORT const char *moe_status_string(int status)
 {

@@ -68,7 +68,7 @@ typedef enum {
     MOE_FP8_E4M3 = 2 /* OCP E4M3, 1 byte (dispatch only: a byte copy)     */
 } moe_dtype;
 
-/* Library ABI version (this header: 1). */
+/* Library ABI version (this header: 2). */
 int moe_version(void);
 
 /* Static text for a status code. */
@@ -171,7 +171,8 @@ int moe_plan_capacity(const int32_t *topk_idx, int64_t S, int K, int E, int64_t 
  *
  * The first call on a device (with that device current) looks up the
  * array's device address once; make that first call before any stream
- * capture.  All calls share the array and it keeps the last call's contents;
+ * capture.  The address is kept for the rest of the process: do not call
+ * cudaDeviceReset on a device after using this entry point on it.  All calls share the array and it keeps the last call's contents;
  * nothing in it needs to start at zero, because each call overwrites every
  * entry it reads.  Calls that overlap on the GPU (e.g. issued on two
  * streams, or from two host threads) race on the array: do not overlap them.
@@ -290,12 +291,17 @@ int moe_plan_dispatch(const int32_t *topk_idx, const void *x, int64_t S, int64_t
  * 16 < K < 32 one pass walks group rows (x[s] is read once per group row);
  * K = 32 takes two passes, the second reading grp_x.
  * max_rows: rows allocated for grp_x (and grp_src/grp_tok_map); must be at
- * least S * min(K, G), which bounds R.  Alignment as moe_dispatch.
+ * least S * min(K, G), which bounds R.
+ * packed_x  [packed_rows, H] of `dtype`: the rows the plan behind grp_tok_map
+ *           addresses (off[E] rows suffice; S*K for moe_plan, E*capacity for
+ *           moe_plan_capacity); a map entry at or past packed_rows is skipped
+ *           and flagged (bit 1 of moe_device_errors).  packed_rows >= 1.
+ * Alignment as moe_dispatch.
  * ---------------------------------------------------------------------- */
 int moe_dispatch_dedup(const void *x, int64_t S, int64_t H, int dtype, int K, int G,
                        const int64_t *goff, const int32_t *grp_src,
                        const int64_t *grp_tok_map, const int64_t *gtok_map,
-                       int64_t max_rows, void *grp_x, void *packed_x,
+                       int64_t max_rows, void *grp_x, void *packed_x, int64_t packed_rows,
                        moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
@@ -333,9 +339,13 @@ int moe_combine(const void *y, int64_t y_rows, int in_dtype, const float *topk_w
  * (the weights of a group row are then read from the token's own row, which
  * is grp_src[r] / K in a plan from moe_group_plan); larger K takes two
  * passes.
+ * y        [y_rows, H] of in_dtype, the expert outputs in the packed order of
+ *          the plan behind grp_tok_map (S*K rows for moe_plan, E*capacity for
+ *          moe_plan_capacity), 1 <= y_rows < 2^31; an entry at or past y_rows
+ *          drops its term and is flagged (bit 2)
  * max_rows >= S * min(K, G).  Alignment as moe_combine.
  * ---------------------------------------------------------------------- */
-int moe_combine_dedup(const void *y, int in_dtype, const float *topk_w,
+int moe_combine_dedup(const void *y, int64_t y_rows, int in_dtype, const float *topk_w,
                       const int64_t *goff, int G, const int32_t *grp_src,
                       const int64_t *grp_tok_map, const int64_t *gtok_map, int64_t S,
                       int64_t H, int K, int64_t max_rows, float *gtok, void *out,

@@ -27,7 +27,7 @@ def test_exports_every_header_function(L):
 
 
 def test_version_and_status_strings(L):
-    assert L.moe_version() == 1
+    assert L.moe_version() == 2
     for s in (0, 1, 2, 3):
         assert L.moe_status_string(s)
     assert b"unknown" in L.moe_status_string(99)
@@ -86,12 +86,13 @@ def test_dispatch_validation(L):
     assert d(px=MIS) == EALIGN
     assert d(ns=48) == EINVAL                # scales without buffers
     assert d(ns=3, xs=FAKE, ps=FAKE) == EALIGN   # 12-byte scale rows
-    assert L.moe_dispatch_dedup(FAKE, 16, 64, 0, 8, 8, FAKE, FAKE, FAKE, FAKE, 100, FAKE, FAKE,
-                                None) == EINVAL  # max_rows < S*min(K,G)
-    assert L.moe_dispatch_dedup(FAKE, 16, 64, 0, 8, 8, FAKE, FAKE, FAKE, None, 128, FAKE, FAKE,
-                                None) == EINVAL  # no gtok_map
-    assert L.moe_dispatch_dedup(FAKE, 16, 64, 0, 8, 8, FAKE, FAKE, FAKE, FAKE, 128, MIS, FAKE,
-                                None) == EALIGN
+    dd = lambda **k: L.moe_dispatch_dedup(FAKE, 16, 64, 0, 8, 8, FAKE, FAKE, FAKE,
+                                          k.get("gtm", FAKE), k.get("mr", 128),
+                                          k.get("gx", FAKE), FAKE, k.get("prows", 128), None)
+    assert dd(mr=100) == EINVAL              # max_rows < S*min(K,G)
+    assert dd(gtm=None) == EINVAL            # no gtok_map
+    assert dd(prows=0) == EINVAL             # no packed rows
+    assert dd(gx=MIS) == EALIGN
 
 
 def test_combine_validation(L):
@@ -107,8 +108,12 @@ def test_combine_validation(L):
     assert c(rows=1 << 31) == EINVAL
     assert c(H=12) == EALIGN
     assert c(out=MIS) == EALIGN
-    assert L.moe_combine_dedup(FAKE, 1, FAKE, FAKE, 8, FAKE, FAKE, FAKE, 16, 64, 8, 127, FAKE,
-                               FAKE, 1, None) == EINVAL
+    cd = lambda **k: L.moe_combine_dedup(FAKE, k.get("rows", 128), 1, FAKE, FAKE, 8, FAKE,
+                                         FAKE, FAKE, 16, 64, 8, k.get("mr", 128), FAKE, FAKE,
+                                         1, None)
+    assert cd(mr=127) == EINVAL              # max_rows < S*min(K,G)
+    assert cd(rows=0) == EINVAL              # no expert rows
+    assert cd(rows=1 << 31) == EINVAL
 
 
 def test_combine_fold_validation(L):

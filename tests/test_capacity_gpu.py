@@ -139,3 +139,81 @@ def test_quantising_dispatch_into_capacity_buckets():
     ref_s = oracle.dispatch(sc0, ref["tok_map"], rows, fill=gpu_path.POISON)
     assert np.array_equal(gpu_path._np(q), ref_q)
     assert np.array_equal(gpu_path._np(sc).view(np.uint32), ref_s.view(np.uint32))
+
+
+def _dedup_over_capacity(wl, gs, cap):
+    """GPU: capacity plan -> group plan -> dedup dispatch -> dedup combine
+    (identity experts: y = the packed rows), every output poisoned first."""
+    import combine_moe_plan_02_gb300 as moe
+    S, K, E, H = wl.S, wl.K, wl.E, wl.H
+    G = E // gs
+    rows = E * cap
+    rmax = max(S * min(K, G), 1)
+    d = gpu_path.to_device(wl)
+    xdt = d["x"].dtype
+    cp = moe.moe_plan_capacity(d["topk_idx"], E, cap)
+    gp = moe.GroupPlan(gpu_path.poisoned((G,), torch.int32), gpu_path.poisoned((G + 1,), torch.int64),
+                       gpu_path.poisoned((S, K), torch.int64), gpu_path.poisoned((rmax,), torch.int32),
+                       gpu_path.poisoned((rmax, K), torch.int64), gs)
+    moe.moe_group_plan(d["topk_idx"], cp.tok_map, E, gs, out=gp)
+    grp_x = gpu_path.poisoned((rmax, H), xdt)
+    packed = gpu_path.poisoned((rows, H), xdt)
+    moe.moe_dispatch_dedup(d["x"], gp, grp_x=grp_x, packed_x=packed)
+    gtok = gpu_path.poisoned((rmax, H), torch.float32)
+    out = gpu_path.poisoned((S, H), xdt)
+    moe.moe_combine_dedup(packed, d["topk_w"], gp, gtok=gtok, out=out, out_dtype=xdt)
+    torch.cuda.synchronize()
+    assert moe.moe_device_errors() == 0
+    R = int(gp.goff[-1].item())
+    np_ = gpu_path._np
+    return dict(tok_map=np_(cp.tok_map), n_dropped=int(cp.n_dropped.item()),
+                gcnt=np_(gp.gcnt), goff=np_(gp.goff), gtok_map=np_(gp.gtok_map),
+                grp_src=np_(gp.grp_src)[:R], grp_tok_map=np_(gp.grp_tok_map)[:R],
+                grp_x=np_(grp_x)[:R], packed=np_(packed), gtok=np_(gtok)[:R], out=np_(out))
+
+
+@pytest.mark.timeout(900)
+@pytest.mark.parametrize("name,S,H,K,gs,cap", [
+    # the dedup shape (f32, 8 groups of 8): E*cap = 34560 rows > S*K, and the
+    # busiest experts drop entries
+    ("dedup", 4096, 4096, 8, 8, 540),
+    # heavy dropping: some group rows lose every expert they stood for
+    ("dedup", 4096, 4096, 8, 8, 300),
+    # bf16; K=12: one-pass dispatch by token, two-pass combine
+    ("moonep", 600, 264, 12, 4, 120),
+    # K=20: dispatch by group row, two-pass combine
+    ("moonep", 500, 136, 20, 8, 170),
+    # K=32: two-pass dispatch and combine
+    ("moonep", 300, 136, 32, 2, 160),
+])
+def test_dedup_over_capacity_plan(name, S, H, K, gs, cap):
+    """The dedup path over a capacity plan's padded rows, against the
+    oracle's capacity plan -> group plan -> dedup dispatch -> dedup combine,
+    bit-exact everywhere (mori #448: op-parity note, capped receive slots with
+    a drop path that writes nothing out of bounds; StdMoE note)."""
+    wl = workloads.make(name, seed=S + cap + K, S=S, H=H, E=64, K=K)
+    rows = wl.E * cap
+    res = _dedup_over_capacity(wl, gs, cap)
+    cp = oracle.plan_capacity(wl.topk_idx, wl.E, cap)
+    assert cp["n_dropped"] > 0 and cp["n_dropped"] == res["n_dropped"]
+    assert np.array_equal(res["tok_map"], cp["tok_map"])
+    assert int(cp["tok_map"].max()) >= S * K or cap * wl.E < S * K
+    gp = oracle.group_plan(wl.topk_idx, cp["tok_map"], wl.E, gs)
+    for key in ("gcnt", "goff", "gtok_map", "grp_src", "grp_tok_map"):
+        assert np.array_equal(res[key], gp[key]), key
+    ogx, opk = oracle.dispatch_dedup(wl.x, gp["grp_src"], gp["grp_tok_map"], K, rows,
+                                     fill=gpu_path.POISON)
+    assert np.array_equal(res["grp_x"], ogx)
+    assert np.array_equal(res["packed"], opk)     # kept rows copied, the rest poisoned
+    dt = "f32" if wl.dtype == "f32" else "bf16"
+    y = np.ascontiguousarray(opk)
+    ogt, oout = oracle.combine_dedup(y, dt, wl.topk_w, gp["grp_src"], gp["grp_tok_map"],
+                                     gp["gtok_map"], H, dt)
+    assert np.array_equal(res["gtok"].view(np.uint32), ogt.view(np.uint32))
+    assert np.array_equal(res["out"].view(np.uint16 if dt == "bf16" else np.uint32),
+                          oout.view(np.uint16 if dt == "bf16" else np.uint32))
+    if gs > 1 and cap <= 300:
+        # group rows none of whose experts kept a slot: copied, summed to zero
+        empty = np.all(gp["grp_tok_map"] < 0, axis=1)
+        assert empty.any()
+        assert np.all(res["gtok"][empty] == 0)

@@ -160,3 +160,34 @@ def test_combine_alternating_K_in_one_process():
         opk = oracle.dispatch(wl.x, p["tok_map"], wl.S * K)
         ref = oracle.combine(opk, "bf16", wl.topk_w, p["tok_map"], wl.H, "bf16")
         assert np.array_equal(np_(out), ref), K
+
+
+@pytest.mark.timeout(900)
+@pytest.mark.parametrize("weighted", [False, True])
+def test_fold_headline_shape(weighted):
+    """The MoonEP shape (S=4096 H=7168 E=64 K=8, bf16, per-expert scales
+    between dispatch and combine), unweighted and weighted, with
+    out_weights: every output element and every folded weight bitwise equal
+    to the oracle's, whose plan, dispatch and expert stage run on their own."""
+    import combine_moe_plan_02_gb300 as moe
+    wl = workloads.make("moonep", seed=0)
+    d = gpu_path.to_device(wl)
+    plan = moe.moe_plan(d["topk_idx"], wl.E)
+    packed = gpu_path.poisoned((wl.S * wl.K, wl.H), torch.bfloat16)
+    moe.moe_dispatch(d["x"], plan.tok_map, packed_x=packed)
+    y = gpu_path.expert_stage(wl, plan, packed, None)
+    out = gpu_path.poisoned((wl.S, wl.H), torch.bfloat16)
+    ow = gpu_path.poisoned((wl.S, wl.K), torch.float32)
+    moe.moe_combine_fold(y, d["topk_w"], plan.tok_map, weighted=weighted, out=out,
+                         out_weights=ow)
+    torch.cuda.synchronize()
+    assert moe.moe_device_errors() == 0
+    p = oracle.plan(wl.topk_idx, wl.E)
+    V = int(p["off"][-1])
+    opk = oracle.dispatch(wl.x, p["tok_map"], V)
+    oy = oracle.expert_scale_bf16(opk, p["off"], wl.expert_scale)
+    assert np.array_equal(np_(y)[:V], oy)
+    ref_out, ref_ow = oracle.combine_fold(oy, "bf16", wl.topk_w, p["tok_map"], wl.H, "bf16",
+                                          weighted=weighted)
+    assert np.array_equal(np_(out), ref_out)
+    assert np.array_equal(np_(ow).view(np.uint32), ref_ow.view(np.uint32))

@@ -2,6 +2,8 @@
 packed rows) against the CPU oracle: codes, scales and untouched rows are
 compared bit-exactly.  The divisions and the cast are IEEE f32 and
 round-to-nearest-even on both sides, so no tolerance is needed."""
+import os
+
 import numpy as np
 import pytest
 
@@ -168,27 +170,40 @@ def test_quantised_dispatch_matches_dispatch_of_quantised_rows():
     assert torch.equal(ps.view(torch.int32), fs.view(torch.int32))
 
 
-@pytest.mark.timeout(600)
-def test_full_size_sampled_tokens():
-    """The benchmarked launch (S=4096 H=7168 E=64 K=8, block 128), checked on
-    a sample of 96 tokens: quantisation is per token row, so the oracle
-    quantises just those rows and each of their K packed rows must match."""
+def _oracle_quant_parallel(x_bf16, block):
+    """oracle.quant_fp8 over row chunks in spawned worker processes (the
+    quantisation is per row, so chunks are independent); the oracle itself
+    stays single-threaded C."""
+    import multiprocessing as mp
+    from concurrent.futures import ProcessPoolExecutor
+    n = max(1, min(16, os.cpu_count() or 1))
+    chunks = [c for c in np.array_split(np.arange(x_bf16.shape[0]), n) if c.size]
+    with ProcessPoolExecutor(len(chunks), mp_context=mp.get_context("spawn")) as ex:
+        parts = list(ex.map(oracle.quant_fp8, [np.ascontiguousarray(x_bf16[c]) for c in chunks],
+                            [block] * len(chunks)))
+    return (np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts]))
+
+
+@pytest.mark.timeout(900)
+def test_full_size_every_token():
+    """The benchmarked launch (S=4096 H=7168 E=64 K=8, block 128): the codes
+    and scales of every token, in each of its K packed rows, equal the
+    oracle's quantisation of that token row."""
     import combine_moe_plan_02_gb300 as moe
     wl = workloads.make("moonep", seed=0)
     dev = torch.device("cuda")
     x = torch.from_numpy(wl.x.view(np.int16)).to(dev).view(torch.bfloat16)
     plan = moe.moe_plan(torch.from_numpy(wl.topk_idx).to(dev), wl.E)
-    q, sc = moe.moe_dispatch_quant_fp8(x, plan.tok_map)
+    q = gpu_path.poisoned((wl.S * wl.K, wl.H), torch.uint8)
+    sc = gpu_path.poisoned((wl.S * wl.K, wl.H // 128), torch.float32)
+    moe.moe_dispatch_quant_fp8(x, plan.tok_map, packed_q=q, packed_scales=sc)
     torch.cuda.synchronize()
     assert moe.moe_device_errors() == 0
     tm = plan.tok_map.cpu().numpy()
     assert np.array_equal(tm, oracle.plan(wl.topk_idx, wl.E)["tok_map"])
-    sample = np.sort(np.random.default_rng(0).choice(wl.S, 96, replace=False))
-    q0, sc0 = oracle.quant_fp8(np.ascontiguousarray(wl.x[sample]), 128)
-    qn = q.view(torch.uint8).cpu().numpy()
-    scn = sc.cpu().numpy()
-    for j, s in enumerate(sample):
-        for k in range(wl.K):
-            r = tm[s, k]
-            assert np.array_equal(qn[r], q0[j]), (s, k)
-            assert np.array_equal(scn[r].view(np.uint32), sc0[j].view(np.uint32)), (s, k)
+    q0, sc0 = _oracle_quant_parallel(wl.x, 128)
+    qn = q.cpu().numpy()
+    scn = sc.cpu().numpy().view(np.uint32)
+    order = tm.reshape(-1)                   # packed row of entry s*K + k
+    assert np.array_equal(qn[order], np.repeat(q0, wl.K, axis=0))
+    assert np.array_equal(scn[order], np.repeat(sc0.view(np.uint32), wl.K, axis=0))

@@ -3,15 +3,19 @@ device workspace (a host linking only this library with no device allocator,
 or a process whose device memory pool forbids further cudaMalloc calls).
 
 It is called here through the C ABI (ctypes, no Python wrapper) and checked
-against moe_plan, which takes a caller-allocated workspace, on two calls in a
-row: the plan is integer work, so the tolerance is exact equality.  The
-second call uses different routing and a different shape, so leftover
-histograms from the first call cannot pass as correct.  This file is named
-to be collected last.
+against the CPU oracle and against moe_plan, which takes a caller-allocated
+workspace, on two calls in a row: the plan is integer work, so the tolerance
+is exact equality.  The second call uses different routing and a different
+shape, so leftover histograms from the first call cannot pass as correct.
+One case enqueues two such calls back to back on one stream with nothing in
+between, the ordering that keeps the second call's histogram kernel from
+overwriting the shared array while the first call's rank kernel reads it.
+This file is named to be collected last.
 """
 import numpy as np
 import pytest
 
+import oracle
 import workloads
 
 torch = pytest.importorskip("torch")
@@ -57,6 +61,44 @@ def test_static_scratch_plan_matches_moe_plan_twice():
             if a.numel() == ref.packed_src.numel():
                 a, b = a[:V], b[:V]
             assert torch.equal(a, b)
+        _check_oracle(got, wl.topk_idx, wl.E)
+
+
+def _check_oracle(got, topk_idx, E):
+    """Every plan output equals the CPU oracle's (plain counting, prefix sum
+    and the (token, k) cursor walk)."""
+    ref = oracle.plan(topk_idx, E)
+    cnt, off, src, tmap, ninv = (t.cpu().numpy() for t in got)
+    V = int(ref["off"][-1])
+    assert np.array_equal(cnt, ref["cnt"])
+    assert np.array_equal(off, ref["off"])
+    assert np.array_equal(src[:V], ref["packed_src"])
+    assert np.array_equal(tmap, ref["tok_map"])
+    assert int(ninv[0]) == ref["n_invalid"]
+
+
+@pytest.mark.timeout(300)
+def test_static_scratch_back_to_back_on_one_stream():
+    """Two large plans of different shapes enqueued one after the other on
+    the same stream, no synchronisation between them, then a third of the
+    first shape: every result equals the oracle's."""
+    import combine_moe_plan_02_gb300 as moe
+    L = moe.lib()
+    dev = torch.device("cuda", 0)
+    wls = [workloads.make("zipf", seed=21, S=18000, H=8, E=256),     # 144000 entries, 71 tiles
+           workloads.make("moonep", seed=22, S=40000, H=8, E=64),    # 320000 entries, 128 tiles
+           workloads.make("zipf", seed=23, S=18000, H=8, E=256)]
+    idxs = [torch.from_numpy(wl.topk_idx).to(dev) for wl in wls]
+    torch.cuda.synchronize()
+    results = []
+    for wl, idx in zip(wls, idxs):
+        rc, got = _static_plan(L, idx, wl.E)     # no synchronisation in between
+        assert rc == 0, L.moe_status_string(rc)
+        results.append(got)
+    torch.cuda.synchronize()
+    assert moe.moe_device_errors() == 0
+    for wl, got in zip(wls, results):
+        _check_oracle(got, wl.topk_idx, wl.E)
 
 
 @pytest.mark.timeout(300)
@@ -73,6 +115,7 @@ def test_static_scratch_single_tile_and_empty():
         torch.cuda.synchronize()
         assert torch.equal(got[0], ref.cnt) and torch.equal(got[1], ref.off)
         assert torch.equal(got[3], ref.tok_map) and torch.equal(got[4], ref.n_invalid)
+        _check_oracle(got, wl.topk_idx, wl.E)
 
 
 @pytest.mark.timeout(300)
