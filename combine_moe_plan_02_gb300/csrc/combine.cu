@@ -253,14 +253,15 @@ __global__ void __launch_bounds__(kThreads, MOE_COMBINE_MIN_BLOCKS) combine_kern
 
 // ---------------------------------------------------------------------------
 // The same sum for the common case -- bf16 rows in and out, weights per
-// output row, K <= 8, no weight fold -- written to hold fewer registers so
-// that more warps fit on an SM and more gathers are in flight: per unit the
-// lanes keep one row pointer each (shuffled to the warp when a step issues
-// its loads) and one ballot of the valid entries instead of K row indices,
-// and each 32-bit word of a gathered vector is widened and added in place.
-// At 72 registers three 256-thread CTAs fit per SM instead of two, and the
-// combine of 4096 rows of 7168 bf16 from K = 8 gathered rows drops from 90
-// to 75 us.  The order of operations is the kernel's above.
+// output row or none, K <= 8, with or without the weight fold -- written to
+// hold fewer registers so that more warps fit on an SM and more gathers are
+// in flight: per unit the lanes keep one row pointer each (shuffled to the
+// warp when a step issues its loads) and one ballot of the valid entries
+// instead of K row indices, and each 32-bit word of a gathered vector is
+// widened and added in place.  At 72 registers three 256-thread CTAs fit per
+// SM instead of two, and the combine of 4096 rows of 7168 bf16 from K = 8
+// gathered rows drops from 90 to 75 us.  The order of operations is the
+// kernel's above, for every mode.
 // ---------------------------------------------------------------------------
 
 #ifndef MOE_COMBINE_LEAN
@@ -270,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, MOE_COMBINE_MIN_BLOCKS) combine_kern
 #define MOE_COMBINE_LEAN_MIN_BLOCKS 3
 #endif
 
+template <bool kWeighted, bool kFold>
 __global__ void __launch_bounds__(kThreads, MOE_COMBINE_LEAN_MIN_BLOCKS)
 combine_lean_kernel(CombineArgs a)
 {
@@ -294,12 +296,20 @@ combine_lean_kernel(CombineArgs a)
             if (r >= 0 && r < a.y_rows) {
                 valid = true;
                 base = a.y + r * row_bytes;
-                w = __ldg(a.w + i * K + lane);
+                if (kWeighted) w = __ldg(a.w + i * K + lane);
             } else if (r != -1) {
                 atomicOr(&g_combine_error, kErrCombineIndex);  // dropped, never gathered
             }
         }
         const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+        if (kFold && sl == 0 && lane < K) {
+            // weight fold: the token's weight vector travels with each of its
+            // valid copies, so entry j accumulates w[i, j] once per copy
+            const float fw = __ldg(a.w + i * K + lane);
+            float acc = 0.0f;
+            for (int c = __popc(vmask); c > 0; --c) acc = __fadd_rn(acc, fw);
+            a.out_w[i * K + lane] = acc;
+        }
         const int64_t pbase = (int64_t)sl * 32 * a.R;
         uint8_t *out_row = a.out + i * row_bytes;
         for (int r = 0; r < a.R; ++r) {
@@ -317,14 +327,20 @@ combine_lean_kernel(CombineArgs a)
             for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
 #pragma unroll
             for (int k = 0; k < kKChunk; ++k) {
-                const float wk = __shfl_sync(0xffffffffu, w, k);
+                const float wk = kWeighted ? __shfl_sync(0xffffffffu, w, k) : 1.0f;
                 if (active && ((vmask >> k) & 1u)) {
                     const uint32_t q[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        acc[2 * e] = __fadd_rn(acc[2 * e], __fmul_rn(wk, __uint_as_float(q[e] << 16)));
-                        acc[2 * e + 1] =
-                            __fadd_rn(acc[2 * e + 1], __fmul_rn(wk, __uint_as_float(q[e] & 0xffff0000u)));
+                        const float lo = __uint_as_float(q[e] << 16);
+                        const float hi = __uint_as_float(q[e] & 0xffff0000u);
+                        if (kWeighted) {
+                            acc[2 * e] = __fadd_rn(acc[2 * e], __fmul_rn(wk, lo));
+                            acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], __fmul_rn(wk, hi));
+                        } else {
+                            acc[2 * e] = __fadd_rn(acc[2 * e], lo);
+                            acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], hi);
+                        }
                     }
                 }
             }
@@ -506,14 +522,16 @@ int launch_combine(CombineArgs &a, int in_dt, int out_dt, int wm, cudaStream_t s
 {
     void (*fn)(CombineArgs) = select_kernel(in_dt, out_dt, wm);
     if (!fn) return MOE_EINVAL;
-    // one cache per (input, output, weight-mode) kernel, one for the lean one
+    // one cache per (input, output, weight-mode) kernel, one per lean one
     static KernelCache caches[2][2][3];
-    static KernelCache lean_cache;
+    static KernelCache lean_cache[2][2];
     KernelCache *cp = &caches[in_dt == MOE_F32][out_dt == MOE_F32][wm];
-    if (MOE_COMBINE_LEAN && in_dt == MOE_BF16 && out_dt == MOE_BF16 && wm == kWeightDirect &&
-        a.K <= kKChunk && !a.out_w && !a.rows_dev) {
-        fn = combine_lean_kernel;
-        cp = &lean_cache;
+    if (MOE_COMBINE_LEAN && in_dt == MOE_BF16 && out_dt == MOE_BF16 &&
+        (wm == kWeightDirect || wm == kUnweighted) && a.K <= kKChunk && !a.rows_dev) {
+        const bool weighted = wm == kWeightDirect, fold = a.out_w != nullptr;
+        fn = weighted ? (fold ? combine_lean_kernel<true, true> : combine_lean_kernel<true, false>)
+                      : (fold ? combine_lean_kernel<false, true> : combine_lean_kernel<false, false>);
+        cp = &lean_cache[weighted][fold];
     }
     KernelCache &cache = *cp;
     int per_sm = 0;

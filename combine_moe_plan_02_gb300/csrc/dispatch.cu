@@ -301,6 +301,68 @@ struct QuantArgs {
 // inlined it would crowd the registers of the common path.
 __device__ __noinline__ float div_rn_out_of_line(float a, float b) { return __fdiv_rn(a, b); }
 
+// The scale of one block and the correctly rounded quotient of an element
+// by it.  Divisions, correctly rounded, by Markstein's correction step
+// (P. Markstein, IBM J. Res. Dev. 34(1), 1990): with y = RN(1/b) and
+// q = RN(a*y), the residual a - q*b is exact under FMA and RN(q + residual*y)
+// = RN(a/b).  The residual is exact only while a is at least 2^-102 (24 bits
+// above the subnormal range); a block whose amax is below 2^-83 can hold
+// elements that small with quotients that still reach an E4M3 code, so such
+// blocks take full divisions instead.
+struct BlockScale {
+    float scale;  // amax / 448, or 1 for an all-zero block
+    float y;      // RN(1 / scale): one reciprocal per block
+    bool slow;    // a block of tiny values: full divisions
+};
+
+__device__ __forceinline__ BlockScale block_scale(float amax)
+{
+    constexpr float kInv448 = 1.0f / 448.0f;  // RN(1/448)
+    const bool exact_fast = amax >= 0x1p-83f;
+    BlockScale b;
+    b.scale = 1.0f;
+    if (exact_fast) {
+        const float q0 = __fmul_rn(amax, kInv448);
+        b.scale = __fmaf_rn(__fmaf_rn(-q0, 448.0f, amax), kInv448, q0);
+    } else if (amax > 0.0f) {
+        b.scale = div_rn_out_of_line(amax, 448.0f);
+    }
+    b.y = __frcp_rn(b.scale);
+    b.slow = amax > 0.0f && !exact_fast;
+    return b;
+}
+
+// RN(x / scale).  A zero residual means q0 is the exact quotient, and
+// returning it keeps the sign of -0.
+__device__ __forceinline__ float quot_rn(float x, const BlockScale &b)
+{
+    if (b.slow) return div_rn_out_of_line(x, b.scale);
+    const float q0 = __fmul_rn(x, b.y);
+    const float r = __fmaf_rn(-q0, b.scale, x);
+    return r == 0.0f ? q0 : __fmaf_rn(r, b.y, q0);
+}
+
+// Four E4M3 codes (nearest even, saturating), little-endian in one word.
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
+{
+    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE,
+                                                             __NV_E4M3);
+    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE,
+                                                             __NV_E4M3);
+    return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+// The 8 bf16 values of a 16-byte word, widened to f32 in element order.
+__device__ __forceinline__ void widen8(const uint4 v, float *f)
+{
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        f[2 * q] = __uint_as_float(w4[q] << 16);
+        f[2 * q + 1] = __uint_as_float(w4[q] & 0xffff0000u);
+    }
+}
+
 // Quantises the 8 bf16 values of one lane (one 16-byte word) for a block of
 // GL lanes: returns the 8 E4M3 codes (little-endian in two words) and the
 // block's scale.  All 32 lanes must call it together (block amax shuffle).
@@ -308,12 +370,7 @@ template <int GL>
 __device__ __forceinline__ uint2 quant8(const uint4 v, bool active, float &scale_out)
 {
     float f[8];
-    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        f[2 * q] = __uint_as_float(w4[q] << 16);
-        f[2 * q + 1] = __uint_as_float(w4[q] & 0xffff0000u);
-    }
+    widen8(v, f);
     float amax = 0.0f;
     if (active) {
 #pragma unroll
@@ -322,44 +379,41 @@ __device__ __forceinline__ uint2 quant8(const uint4 v, bool active, float &scale
 #pragma unroll
     for (int o = GL / 2; o > 0; o >>= 1)
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    // Divisions, correctly rounded, by Markstein's correction step
-    // (P. Markstein, IBM J. Res. Dev. 34(1), 1990): with y = RN(1/b) and
-    // q = RN(a*y), the residual a - q*b is exact under FMA and
-    // RN(q + residual*y) = RN(a/b).  The residual is exact only while a is
-    // at least 2^-102 (24 bits above the subnormal range); a block whose
-    // amax is below 2^-83 can hold elements that small with quotients that
-    // still reach an E4M3 code, so such blocks take full divisions instead.
-    constexpr float kInv448 = 1.0f / 448.0f;  // RN(1/448)
-    const bool exact_fast = amax >= 0x1p-83f;
-    float scale = 1.0f;
-    if (exact_fast) {
-        const float q0 = __fmul_rn(amax, kInv448);
-        scale = __fmaf_rn(__fmaf_rn(-q0, 448.0f, amax), kInv448, q0);
-    } else if (amax > 0.0f) {
-        scale = div_rn_out_of_line(amax, 448.0f);
-    }
-    // one reciprocal per block instead of a full division per element; a
-    // zero residual means q0 is the exact quotient, and returning it keeps
-    // the sign of -0
-    const float y = __frcp_rn(scale);
-    const bool slow = amax > 0.0f && !exact_fast;
-    auto quot = [&](float x) {
-        if (slow) return div_rn_out_of_line(x, scale);
-        const float q0 = __fmul_rn(x, y);
-        const float r = __fmaf_rn(-q0, scale, x);
-        return r == 0.0f ? q0 : __fmaf_rn(r, y, q0);
-    };
+    const BlockScale b = block_scale(amax);
     uint32_t packed[2];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-            make_float2(quot(f[4 * q]), quot(f[4 * q + 1])), __NV_SATFINITE, __NV_E4M3);
-        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-            make_float2(quot(f[4 * q + 2]), quot(f[4 * q + 3])), __NV_SATFINITE, __NV_E4M3);
-        packed[q] = (uint32_t)lo | ((uint32_t)hi << 16);
-    }
-    scale_out = scale;
+    for (int q = 0; q < 2; ++q)
+        packed[q] = e4m3x4(quot_rn(f[4 * q], b), quot_rn(f[4 * q + 1], b),
+                           quot_rn(f[4 * q + 2], b), quot_rn(f[4 * q + 3], b));
+    scale_out = b.scale;
     return make_uint2(packed[0], packed[1]);
+}
+
+// The same for the 16 bf16 values of two consecutive 16-byte words (a block
+// spans GL lanes of 16 elements): 16 codes in one 16-byte word.
+template <int GL>
+__device__ __forceinline__ uint4 quant16(const uint4 v0, const uint4 v1, bool active,
+                                         float &scale_out)
+{
+    float f[16];
+    widen8(v0, f);
+    widen8(v1, f + 8);
+    float amax = 0.0f;
+    if (active) {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) amax = fmaxf(amax, fabsf(f[q]));
+    }
+#pragma unroll
+    for (int o = GL / 2; o > 0; o >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const BlockScale b = block_scale(amax);
+    uint32_t packed[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        packed[q] = e4m3x4(quot_rn(f[4 * q], b), quot_rn(f[4 * q + 1], b),
+                           quot_rn(f[4 * q + 2], b), quot_rn(f[4 * q + 3], b));
+    scale_out = b.scale;
+    return make_uint4(packed[0], packed[1], packed[2], packed[3]);
 }
 
 template <int GL>  // lanes per block (block / 8)
@@ -594,6 +648,120 @@ __global__ void __launch_bounds__(kQBWarps * 32) dispatch_quant_bulk_kernel(QBul
     }
 }
 
+// ---------------------------------------------------------------------------
+// Quantising dispatch, wide form (the common case: every chunk's scale run is
+// a whole number of 16-byte words, H a multiple of 4 * block, and the scale
+// buffer 16-byte aligned).  A warp owns (token, 1024-element chunk) units;
+// each lane quantises 16 consecutive elements per 512-element step, so that
+// its 16 codes leave as ONE 16-byte store per destination row (a warp store
+// covers 512 contiguous bytes), and the chunk's scale run (4 to 64 floats) is
+// collected in shared memory and leaves as 16-byte stores of whole words.
+// All of a unit's loads (4 x 16 bytes per lane) are issued first.  No
+// mbarrier, no bulk-copy engine: the stores go straight from registers, and
+// at 64 registers per thread 32 warps fit on an SM.
+// ---------------------------------------------------------------------------
+
+#ifndef MOE_QUANT_WIDE
+#define MOE_QUANT_WIDE 1
+#endif
+#ifndef MOE_QW_STORE_CS
+#define MOE_QW_STORE_CS 1
+#endif
+constexpr int kQWThreads = 256;
+constexpr int kQWWarps = kQWThreads / 32;
+constexpr int kQWChunk = 1024;            // elements per unit (2 steps of 512)
+
+struct QWideArgs {
+    const uint8_t *x;         // bf16 [S, H]
+    int64_t S, H;
+    int K;
+    const int64_t *tok_map;   // [S, K]
+    int64_t dst_rows;
+    int block;
+    int64_t nb;               // scales per row, H / block (a multiple of 4)
+    int n_chunks;             // units per row
+    uint8_t *q;               // [dst_rows, H]
+    float *sc;                // [dst_rows, nb], 16-byte aligned
+};
+
+__device__ __forceinline__ void st16_q(void *p, uint4 v)
+{
+#if MOE_QW_STORE_CS
+    st16_cs(p, v);
+#else
+    st16(p, v);
+#endif
+}
+
+template <int GL>  // lanes per block (block / 16)
+__global__ void __launch_bounds__(kQWThreads, 4) dispatch_quant_wide_kernel(QWideArgs a)
+{
+    __shared__ __align__(16) float s_sc[kQWWarps][kQWChunk / 16];  // a unit's scale run
+
+    griddep_wait();  // the plan and earlier readers of the packed buffers are done
+    griddep_launch_dependents();
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t gw = (int64_t)blockIdx.x * kQWWarps + warp;
+    const int64_t W = (int64_t)gridDim.x * kQWWarps;
+    const int64_t units = a.S * a.n_chunks;
+    const int K = a.K;
+    float *my_sc = s_sc[warp];
+
+    for (int64_t u = gw; u < units; u += W) {
+        const int64_t s = u / a.n_chunks;
+        const int c = (int)(u - s * a.n_chunks);
+        const int64_t e0 = (int64_t)c * kQWChunk;
+        const int elems = (int)min((int64_t)kQWChunk, a.H - e0);  // a multiple of 4 * block
+        int32_t my_row = -1;
+        if (lane < K) {
+            const int64_t r = __ldg(a.tok_map + s * K + lane);
+            if (r >= 0 && r < a.dst_rows)
+                my_row = (int32_t)r;
+            else if (r != -1)
+                atomicOr(&g_dispatch_error, kErrDispatchIndex);
+        }
+        // load first: both steps' 32 bytes per lane are in flight together
+        const uint8_t *src = a.x + (s * a.H + e0) * 2;
+        uint4 v[2][2];
+        bool act[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int e = t * 512 + lane * 16;
+            act[t] = e < elems;
+            if (act[t]) {
+                v[t][0] = ld_stream16(src + e * 2);
+                v[t][1] = ld_stream16(src + e * 2 + 16);
+            } else {
+                v[t][0] = v[t][1] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        uint4 codes[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            float scale;
+            codes[t] = quant16<GL>(v[t][0], v[t][1], act[t], scale);
+            const int e = t * 512 + lane * 16;
+            if (act[t] && (lane % GL) == 0) my_sc[e / a.block] = scale;
+        }
+        __syncwarp();
+        const int nsc = elems / a.block;            // scales of this unit
+        const bool sc_lane = lane * 4 < nsc;
+        uint4 scw = make_uint4(0, 0, 0, 0);
+        if (sc_lane) scw = *reinterpret_cast<const uint4 *>(my_sc + lane * 4);
+        __syncwarp();                                // my_sc is rewritten by the next unit
+        for (int k = 0; k < K; ++k) {
+            const int32_t d = __shfl_sync(0xffffffffu, my_row, k);
+            if (d < 0) continue;                     // the same for every lane
+            uint8_t *dq = a.q + (int64_t)d * a.H + e0;
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+                if (act[t]) st16_q(dq + t * 512 + lane * 16, codes[t]);
+            if (sc_lane) st16_q(a.sc + (int64_t)d * a.nb + e0 / a.block + lane * 4, scw);
+        }
+    }
+}
+
 int pick_chunk(int64_t row_bytes, int *n_chunks)
 {
     // split the row into m equal chunks of at most kMaxChunk bytes when the
@@ -748,6 +916,55 @@ MOE_EXPORT int moe_dispatch_dedup(const void *x, int64_t S, int64_t H, int dtype
     return launch_copy(a, (cudaStream_t)stream);
 }
 
+namespace moe {
+namespace {
+int launch_quant_wide(const void *x, int64_t S, int64_t H, int K, const int64_t *tok_map,
+                      int block, void *packed_q, float *packed_scales, int64_t packed_rows,
+                      cudaStream_t stream)
+{
+    QWideArgs a = {};
+    a.x = static_cast<const uint8_t *>(x);
+    a.S = S;
+    a.H = H;
+    a.K = K;
+    a.tok_map = tok_map;
+    a.dst_rows = packed_rows;
+    a.block = block;
+    a.nb = H / block;
+    a.n_chunks = (int)((H + kQWChunk - 1) / kQWChunk);
+    a.q = static_cast<uint8_t *>(packed_q);
+    a.sc = packed_scales;
+    void (*fn)(QWideArgs) = nullptr;
+    static KernelCache caches[5];
+    KernelCache *cache = nullptr;
+    switch (block) {
+    case 16: fn = dispatch_quant_wide_kernel<1>; cache = &caches[0]; break;
+    case 32: fn = dispatch_quant_wide_kernel<2>; cache = &caches[1]; break;
+    case 64: fn = dispatch_quant_wide_kernel<4>; cache = &caches[2]; break;
+    case 128: fn = dispatch_quant_wide_kernel<8>; cache = &caches[3]; break;
+    default: fn = dispatch_quant_wide_kernel<16>; cache = &caches[4]; break;
+    }
+    int per_sm = 0;
+    cudaError_t err = prepare_kernel(fn, 0, kQWThreads, *cache, &per_sm);
+    if (err != cudaSuccess || per_sm < 1) {
+        set_cuda_error(err != cudaSuccess ? err : cudaErrorInvalidConfiguration);
+        return MOE_ECUDA;
+    }
+    const int64_t units = S * a.n_chunks;
+    int64_t blocks = (units + kQWWarps - 1) / kQWWarps;
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    err = launch_pdl(fn, dim3((unsigned)blocks), dim3(kQWThreads), 0, stream, a);
+    if (err != cudaSuccess) {
+        set_cuda_error(err);
+        return MOE_ECUDA;
+    }
+    return check_launch();
+}
+} // namespace
+} // namespace moe
+
 #if MOE_QUANT_BULK
 namespace moe {
 namespace {
@@ -814,6 +1031,9 @@ MOE_EXPORT int moe_dispatch_quant_fp8(const void *x, int64_t S, int64_t H, int K
     if (!x || !tok_map || !packed_q || !packed_scales || packed_rows < 1) return MOE_EINVAL;
     if (!aligned16(x) || !aligned16(packed_q) || (reinterpret_cast<uintptr_t>(packed_scales) & 3u))
         return MOE_EALIGN;
+    if (MOE_QUANT_WIDE && H % (4 * block) == 0 && aligned16(packed_scales))
+        return launch_quant_wide(x, S, H, K, tok_map, block, packed_q, packed_scales,
+                                 packed_rows, (cudaStream_t)stream);
 #if MOE_QUANT_BULK
     if (H % (4 * block) == 0 && aligned16(packed_scales))
         return launch_quant_bulk(x, S, H, K, tok_map, block, packed_q, packed_scales,
