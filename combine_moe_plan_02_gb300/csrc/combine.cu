@@ -14,8 +14,9 @@
 // shuffled to all lanes), then per step issues all K 16-byte gathers before
 // the first add (load first), accumulates in f32 in increasing k with a
 // separately rounded multiply and add, and stores the rounded result with
-// one 16-byte store.  A persistent grid sized to the SM count strides over
-// units.  There is no shared memory, no atomics and no inter-CTA wait.
+// one 16-byte store.  The grid holds several resident waves of CTAs whose
+// warps stride over units (see MOE_COMBINE_GRID_WAVES).  There is no shared
+// memory, no atomics and no inter-CTA wait.
 //
 // Weight fold (mori #448, the note on reducing the K forwarded per-token
 // weight vectors into out_weights, folded into the gather at part 0): the
@@ -39,6 +40,18 @@ constexpr int kKChunk = 8;   // map entries held in registers at a time
 #define MOE_COMBINE_LANE_STEPS 4
 #endif
 constexpr int kMaxLaneSteps = MOE_COMBINE_LANE_STEPS;  // 8-element steps per lane per unit
+// Grid size in resident waves (CTAs per SM x SMs x waves).  SMs of this part
+// do not move data at the same rate (per-SM times of one equal share measured
+// 51 to 82 us in the dispatch, the same SMs slow on every launch), so a grid
+// of several waves of short CTAs, which the block scheduler hands to
+// whichever SM frees up, beats a persistent grid whose warps stride over a
+// fixed share: at S=4096 H=7168 K=8 the combine inside the step (after the
+// dispatch) went 92.9 -> 90.1 us and the step 181.8 -> 179.4 us, for 74.7 ->
+// 77.9 us when timed alone.  Handing the units out through a global counter
+// instead measured slower (atomic latency under the write traffic).
+#ifndef MOE_COMBINE_GRID_WAVES
+#define MOE_COMBINE_GRID_WAVES 8
+#endif
 
 enum WMode { kWeightDirect = 0, kWeightViaSrc = 1, kUnweighted = 2 };
 
@@ -504,7 +517,7 @@ void (*select_kernel(int in_dt, int out_dt, int wm))(CombineArgs)
 void set_slices(CombineArgs &a, int64_t warp_slots)
 {
     // slices: at most kMaxLaneSteps steps per lane per unit, slices of equal
-    // size; finer units even out the work of the persistent warps.  When the
+    // size; finer units even out the work of the warps.  When the
     // rows cannot fill every warp of the grid (small batches), rows are cut
     // finer, down to one step per lane, so that more gathers are in flight
     // at once; the summation order of an element never depends on this.
@@ -543,7 +556,7 @@ int launch_combine(CombineArgs &a, int in_dt, int out_dt, int wm, cudaStream_t s
     set_slices(a, (int64_t)sm_count() * per_sm * (kThreads / 32));
     const int64_t units = a.rows * a.slices;
     int64_t blocks = (units + kThreads / 32 - 1) / (kThreads / 32);
-    const int64_t cap = (int64_t)sm_count() * per_sm;
+    const int64_t cap = (int64_t)sm_count() * per_sm * MOE_COMBINE_GRID_WAVES;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     err = launch_pdl(fn, dim3((unsigned)blocks), dim3(kThreads), 0, stream, a);
@@ -580,7 +593,7 @@ int launch_dedup(DedupArgs &d, int in_dt, int out_dt, cudaStream_t stream)
     d.slices = geo.slices;
     const int64_t units = d.S * d.slices;
     int64_t blocks = (units + kThreads / 32 - 1) / (kThreads / 32);
-    const int64_t cap = (int64_t)sm_count() * per_sm;
+    const int64_t cap = (int64_t)sm_count() * per_sm * MOE_COMBINE_GRID_WAVES;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     err = launch_pdl(fn, dim3((unsigned)blocks), dim3(kThreads), 0, stream, d);

@@ -34,6 +34,14 @@ namespace {
 #ifndef MOE_DISPATCH_CHUNK
 #define MOE_DISPATCH_CHUNK 4096
 #endif
+// Grid size in resident waves.  With one wave (a persistent grid) every warp
+// owns a fixed share of the chunks and the slowest SMs set the pace; with
+// eight, the block scheduler keeps handing CTAs to the SMs that finish
+// first: 89.0 -> 81.9 us at S=4096 H=7168 K=8 (each warp then mostly moves
+// one chunk through its ring).
+#ifndef MOE_DISPATCH_GRID_WAVES
+#define MOE_DISPATCH_GRID_WAVES 8
+#endif
 constexpr int kWarpsPerCta = MOE_DISPATCH_WARPS;
 constexpr int kStages = MOE_DISPATCH_STAGES;
 constexpr int kMaxChunk = MOE_DISPATCH_CHUNK;  // bytes of a row moved per stage
@@ -667,6 +675,11 @@ __global__ void __launch_bounds__(kQBWarps * 32) dispatch_quant_bulk_kernel(QBul
 #ifndef MOE_QW_STORE_CS
 #define MOE_QW_STORE_CS 1
 #endif
+// Grid size in resident waves, as MOE_DISPATCH_GRID_WAVES: 55.0 -> 51.2 us
+// at S=4096 H=7168 K=8 with four waves instead of one.
+#ifndef MOE_QW_GRID_WAVES
+#define MOE_QW_GRID_WAVES 4
+#endif
 constexpr int kQWThreads = 256;
 constexpr int kQWWarps = kQWThreads / 32;
 constexpr int kQWChunk = 1024;            // elements per unit (2 steps of 512)
@@ -791,7 +804,7 @@ int launch_copy(CopyArgs &a, cudaStream_t stream)
     }
     const int64_t items = a.rows * a.n_chunks;
     int64_t blocks = (items + kWarpsPerCta - 1) / kWarpsPerCta;
-    const int64_t cap = (int64_t)sm_count() * per_sm;
+    const int64_t cap = (int64_t)sm_count() * per_sm * MOE_DISPATCH_GRID_WAVES;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     err = launch_pdl(dispatch_bulk_kernel, dim3((unsigned)blocks), dim3(kWarpsPerCta * 32), smem,
@@ -952,7 +965,7 @@ int launch_quant_wide(const void *x, int64_t S, int64_t H, int K, const int64_t 
     }
     const int64_t units = S * a.n_chunks;
     int64_t blocks = (units + kQWWarps - 1) / kQWWarps;
-    const int64_t cap = (int64_t)sm_count() * per_sm;
+    const int64_t cap = (int64_t)sm_count() * per_sm * MOE_QW_GRID_WAVES;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     err = launch_pdl(fn, dim3((unsigned)blocks), dim3(kQWThreads), 0, stream, a);
