@@ -707,13 +707,17 @@ def run_ours(args):
     nby = algorithmic_bytes(S, H, E, K, V)
     step_bytes = sum(nby.values())
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    # the rule moe_plan_dispatch applies: one launch up to 1024 entries, or
+    # up to 131072 entries with at most 1024 per SM's token range and at most
+    # 384 MiB of rows to copy; else moe_plan then moe_dispatch
     one_launch = (S * K <= int(moe.lib().moe_plan_dispatch_fused_max())
-                  or (S * K <= 131072 and -(-S // n_sm) * K <= 1024))
+                  or (S * K <= 131072 and -(-S // n_sm) * K <= 1024
+                      and S * K * H * 2 <= (384 << 20)))
     launches_per_step = (1 if one_launch else
                          (2 if moe.moe_plan_workspace_size(S, K, E) > 0 else 1) + 1) + 1
 
     def step():
-        # plan + dispatch in one launch (moe_plan_dispatch), then combine
+        # plan + dispatch (moe_plan_dispatch: one launch or two), then combine
         moe.moe_plan_dispatch(idx, x, E, out=plan, packed_x=packed, workspace=ws, stream=stream)
         moe.moe_combine(y, w, plan.tok_map, out=out, stream=stream)
 
@@ -855,13 +859,18 @@ def run_ours(args):
                                                 step_bytes, world, idx, w, d_x16, out)
 
     peak, peak_kind = read_peaks()
-    # the roofline kernel: the slower of the step's two launches, timed as
-    # they run in the step (timed region 2b)
-    pd_ms = statistics.mean(t_pd)
-    comb_ms = statistics.mean(t_pd_comb)
-    dom = "plan_dispatch" if pd_ms >= comb_ms else "combine"
-    dom_ms = pd_ms if dom == "plan_dispatch" else comb_ms
-    dom_bytes = nby["plan"] + nby["dispatch"] if dom == "plan_dispatch" else nby["combine"]
+    # the roofline kernel: the slowest of the step's launches, timed as they
+    # run in the step -- the one-launch plan + dispatch and the combine
+    # (timed region 2b), or plan, dispatch and combine (timed region 2)
+    if one_launch:
+        cand = {"plan_dispatch": (statistics.mean(t_pd), nby["plan"] + nby["dispatch"]),
+                "combine": (statistics.mean(t_pd_comb), nby["combine"])}
+    else:
+        cand = {"plan": (statistics.mean(t_plan), nby["plan"]),
+                "dispatch": (statistics.mean(t_disp), nby["dispatch"]),
+                "combine": (statistics.mean(t_comb), nby["combine"])}
+    dom = max(cand, key=lambda k_: cand[k_][0])
+    dom_ms, dom_bytes = cand[dom]
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
 
     def percall(name, ts, nbytes=None):
@@ -883,14 +892,16 @@ def run_ours(args):
                    "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write + "
                          f"{L2_FLUSH_BYTES >> 20} MiB read, untimed)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "step": "moe_plan_dispatch (plan + dispatch, one launch) + moe_combine"},
+                   "step": "moe_plan_dispatch (plan + dispatch: " +
+                           ("one launch" if one_launch else "moe_plan then moe_dispatch, two launches") +
+                           ") + moe_combine"},
         "per_call": {"plan": percall("plan", t_plan), "dispatch": percall("dispatch", t_disp),
                      "combine": percall("combine", t_comb),
                      "plan_dispatch": percall("plan_dispatch", t_pd,
                                               nby["plan"] + nby["dispatch"]),
                      "combine_in_step": percall("combine", t_pd_comb),
                      "what": "plan, dispatch, combine: the three calls one after another; "
-                             "plan_dispatch, combine_in_step: the step's two launches"},
+                             "plan_dispatch, combine_in_step: the step's two calls"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                      "algorithmic_bytes": dom_bytes, "us": round(1e3 * dom_ms, 2),
                      "peak": peak, "peak_kind": f"{peak_kind} copy bandwidth (burst)",

@@ -277,17 +277,17 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) dispatch_bulk_kernel(CopyAr
 // code = E4M3(v / scale), both divisions IEEE f32, the cast to nearest even
 // and saturating.
 //
-// A warp owns (token, slice) units: each lane holds 8 consecutive elements
-// (one 16-byte load), a block of `block` elements spans block/8 lanes, and
-// its amax is an xor-shuffle reduction inside that lane group.  All of a
-// unit's loads are issued first.  Each lane then stores its 8 codes (8
-// bytes; a warp writes 256 contiguous bytes) to every destination row, and
-// the first lane of each block stores the block's scale.
+// Two kernels compute the same bits: the wide kernel further down takes the
+// common case (H a multiple of 4 * block, 16-byte aligned scales); the
+// register kernel here takes every other shape.  It gives a warp (token,
+// slice) units: each lane holds 8 consecutive elements (one 16-byte load), a
+// block of `block` elements spans block/8 lanes, and its amax is an
+// xor-shuffle reduction inside that lane group.  All of a unit's loads are
+// issued first.  Each lane then stores its 8 codes (8 bytes; a warp writes
+// 256 contiguous bytes) to every destination row, and the first lane of each
+// block stores the block's scale.
 // ---------------------------------------------------------------------------
 
-#ifndef MOE_QUANT_BULK
-#define MOE_QUANT_BULK 1
-#endif
 constexpr int kQThreads = 256;
 constexpr int kQMaxIters = 8;  // 256-element steps per lane group per unit
 
@@ -482,181 +482,6 @@ __global__ void __launch_bounds__(kQThreads, 2) dispatch_quant_kernel(QuantArgs 
 }
 
 // ---------------------------------------------------------------------------
-// Quantising dispatch through shared memory.  Each token row is quantised
-// once: a warp pulls a 1024-element chunk of bf16 into a stage with a bulk
-// copy, its 32 lanes quantise it (256 elements per step, as above) into the
-// stage's code and scale areas, and lanes 0..K-1 push those to the K
-// destination rows with bulk copies -- the same ring as dispatch_bulk_kernel,
-// with the per-destination work reduced to two bulk stores.  Used when every
-// chunk's scale run is a whole number of 16-byte words (H a multiple of
-// 4 * block) and the scale buffer is 16-byte aligned.
-// ---------------------------------------------------------------------------
-
-#ifndef MOE_QB_CHUNK
-#define MOE_QB_CHUNK 1024
-#endif
-constexpr int kQBChunk = MOE_QB_CHUNK;                           // elements per stage
-constexpr int kQBStageBytes = kQBChunk * 2 + kQBChunk + kQBChunk / 16 * 4;  // in, codes, scales
-#ifndef MOE_QB_STAGES
-#define MOE_QB_STAGES 2
-#endif
-#ifndef MOE_QB_WARPS
-#define MOE_QB_WARPS 4
-#endif
-#ifndef MOE_QB_GROUP
-#define MOE_QB_GROUP 2
-#endif
-constexpr int kQBStages = MOE_QB_STAGES;
-constexpr int kQBWarps = MOE_QB_WARPS;
-constexpr int kQBGroup = MOE_QB_GROUP;   // 256-element steps quantised together
-// The quantisation is latency-bound (shuffle and division chains), so resident
-// warps matter more than ring depth: two 1024-element stages per warp leave
-// room for 32 warps per SM (55 us at the MoonEP shape), where four
-// 2048-element stages allowed 8 (75-90 us).
-
-struct QBulkArgs {
-    const uint8_t *x;         // bf16 [S, H]
-    int64_t S, H;
-    int K;
-    const int64_t *tok_map;   // [S, K]
-    int64_t dst_rows;
-    int block;
-    int64_t nb;               // scales per row, H / block
-    int n_chunks;             // chunks per row
-    uint8_t *q;               // [dst_rows, H]
-    uint8_t *sc;              // f32 [dst_rows, nb]
-};
-
-template <int GL>
-__global__ void __launch_bounds__(kQBWarps * 32) dispatch_quant_bulk_kernel(QBulkArgs a)
-{
-    extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(8) uint64_t bars[kQBWarps][kQBStages];
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint8_t *ring = smem + (size_t)warp * kQBStages * kQBStageBytes;
-    uint64_t *bar = bars[warp];
-
-    if (lane == 0) {
-        for (int st = 0; st < kQBStages; ++st) mbar_init(&bar[st], 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
-
-    griddep_wait();  // the plan and earlier readers of the packed buffers are done
-    griddep_launch_dependents();
-
-    const int64_t n_items = a.S * a.n_chunks;
-    const int64_t gw = (int64_t)blockIdx.x * kQBWarps + warp;
-    const int64_t W = (int64_t)gridDim.x * kQBWarps;
-    if (gw >= n_items) return;
-    const int64_t n_mine = (n_items - gw + W - 1) / W;
-
-    int64_t dst_row[kQBStages];
-    int64_t issued = 0;
-
-    auto issue = [&](int64_t j, int st) {
-        issued = j + 1;
-        const int64_t it = gw + j * W;
-        const int64_t r = it / a.n_chunks;
-        const int c = (int)(it - r * a.n_chunks);
-        const int64_t e0 = (int64_t)c * kQBChunk;
-        const uint32_t elems = (uint32_t)min((int64_t)kQBChunk, a.H - e0);
-        if (lane == 0) {
-            uint8_t *stage = ring + (size_t)st * kQBStageBytes;
-            fence_proxy_async_smem();  // earlier reads of the stage come first
-            mbar_arrive_expect_tx(&bar[st], elems * 2);
-            bulk_g2s(stage, a.x + (r * a.H + e0) * 2, elems * 2, &bar[st]);
-        }
-        int64_t d = -1;
-        if (lane < a.K) d = __ldg(a.tok_map + r * a.K + lane);
-        if (d >= a.dst_rows || d < -1) {
-            atomicOr(&g_dispatch_error, kErrDispatchIndex);
-            d = -1;
-        }
-        dst_row[st] = d;
-    };
-
-#pragma unroll
-    for (int st = 0; st < kQBStages; ++st)
-        if (st < n_mine) issue(st, st);
-
-    bool ok = true;
-    int64_t consumed = 0;
-    for (int64_t j0 = 0; j0 < n_mine && ok; j0 += kQBStages) {
-#pragma unroll
-        for (int st = 0; st < kQBStages; ++st) {
-            const int64_t j = j0 + st;
-            if (j >= n_mine || !ok) break;
-            const bool landed = mbar_wait_bounded(&bar[st], (uint32_t)((j / kQBStages) & 1));
-            if (!__all_sync(0xffffffffu, landed)) {
-                ok = false;
-                break;
-            }
-            consumed = j + 1;
-            const int64_t it = gw + j * W;
-            const int64_t r = it / a.n_chunks;
-            const int c = (int)(it - r * a.n_chunks);
-            const int64_t e0 = (int64_t)c * kQBChunk;
-            const int elems = (int)min((int64_t)kQBChunk, a.H - e0);
-            uint8_t *in = ring + (size_t)st * kQBStageBytes;
-            uint8_t *codes = in + kQBChunk * 2;
-            float *scs = reinterpret_cast<float *>(codes + kQBChunk);
-            // kQBGroup independent 256-element steps at a time, so that their
-            // shuffle and division chains overlap; steps past a short last
-            // chunk run on zeros and store nothing
-#pragma unroll
-            for (int t0 = 0; t0 < kQBChunk / 256; t0 += kQBGroup) {
-                uint4 v[kQBGroup];
-                bool act[kQBGroup];
-#pragma unroll
-                for (int u = 0; u < kQBGroup; ++u) {
-                    const int e = (t0 + u) * 256 + lane * 8;
-                    act[u] = e < elems;
-                    v[u] = act[u] ? *reinterpret_cast<const uint4 *>(in + e * 2)
-                                  : make_uint4(0, 0, 0, 0);
-                }
-                float scale[kQBGroup];
-                uint2 cw[kQBGroup];
-#pragma unroll
-                for (int u = 0; u < kQBGroup; ++u) cw[u] = quant8<GL>(v[u], act[u], scale[u]);
-#pragma unroll
-                for (int u = 0; u < kQBGroup; ++u) {
-                    const int e = (t0 + u) * 256 + lane * 8;
-                    if (act[u]) {
-                        *reinterpret_cast<uint2 *>(codes + e) = cw[u];
-                        if ((lane % GL) == 0) scs[e / a.block] = scale[u];
-                    }
-                }
-            }
-            fence_proxy_async_smem();  // the codes and scales are visible to the bulk stores
-            __syncwarp();
-            const int64_t d = dst_row[st];
-            if (d >= 0) {
-                bulk_s2g(a.q + d * a.H + e0, codes, (uint32_t)elems);
-                bulk_s2g(a.sc + (d * a.nb + e0 / a.block) * 4, scs,
-                         (uint32_t)(elems / a.block) * 4);
-            }
-            bulk_commit();
-            const int prev = (st + kQBStages - 1) % kQBStages;
-            const int64_t jn = j - 1 + kQBStages;
-            if (j >= 1 && jn < n_mine) {
-                bulk_wait_read<1>();
-                __syncwarp();
-                issue(jn, prev);
-            }
-        }
-    }
-
-    bulk_wait_all();
-    if (!ok) {
-        if (lane == 0) atomicOr(&g_dispatch_error, kErrDispatchTimeout);
-        for (int64_t j = consumed; j < issued; ++j)
-            (void)mbar_wait_bounded(&bar[j % kQBStages], (uint32_t)((j / kQBStages) & 1));
-    }
-}
-
-// ---------------------------------------------------------------------------
 // Quantising dispatch, wide form (the common case: every chunk's scale run is
 // a whole number of 16-byte words, H a multiple of 4 * block, and the scale
 // buffer 16-byte aligned).  A warp owns (token, 1024-element chunk) units;
@@ -669,9 +494,6 @@ __global__ void __launch_bounds__(kQBWarps * 32) dispatch_quant_bulk_kernel(QBul
 // at 64 registers per thread 32 warps fit on an SM.
 // ---------------------------------------------------------------------------
 
-#ifndef MOE_QUANT_WIDE
-#define MOE_QUANT_WIDE 1
-#endif
 #ifndef MOE_QW_STORE_CS
 #define MOE_QW_STORE_CS 1
 #endif
@@ -978,58 +800,6 @@ int launch_quant_wide(const void *x, int64_t S, int64_t H, int K, const int64_t 
 } // namespace
 } // namespace moe
 
-#if MOE_QUANT_BULK
-namespace moe {
-namespace {
-int launch_quant_bulk(const void *x, int64_t S, int64_t H, int K, const int64_t *tok_map,
-                      int block, void *packed_q, float *packed_scales, int64_t packed_rows,
-                      cudaStream_t stream)
-{
-    QBulkArgs a = {};
-    a.x = static_cast<const uint8_t *>(x);
-    a.S = S;
-    a.H = H;
-    a.K = K;
-    a.tok_map = tok_map;
-    a.dst_rows = packed_rows;
-    a.block = block;
-    a.nb = H / block;
-    a.n_chunks = (int)((H + kQBChunk - 1) / kQBChunk);
-    a.q = static_cast<uint8_t *>(packed_q);
-    a.sc = reinterpret_cast<uint8_t *>(packed_scales);
-    void (*fn)(QBulkArgs) = nullptr;
-    static KernelCache caches[5];
-    KernelCache *cache = nullptr;
-    switch (block) {
-    case 16: fn = dispatch_quant_bulk_kernel<2>; cache = &caches[0]; break;
-    case 32: fn = dispatch_quant_bulk_kernel<4>; cache = &caches[1]; break;
-    case 64: fn = dispatch_quant_bulk_kernel<8>; cache = &caches[2]; break;
-    case 128: fn = dispatch_quant_bulk_kernel<16>; cache = &caches[3]; break;
-    default: fn = dispatch_quant_bulk_kernel<32>; cache = &caches[4]; break;
-    }
-    const size_t smem = (size_t)kQBWarps * kQBStages * kQBStageBytes;
-    int per_sm = 0;
-    cudaError_t err = prepare_kernel(fn, smem, kQBWarps * 32, *cache, &per_sm);
-    if (err != cudaSuccess || per_sm < 1) {
-        set_cuda_error(err != cudaSuccess ? err : cudaErrorInvalidConfiguration);
-        return MOE_ECUDA;
-    }
-    const int64_t items = S * a.n_chunks;
-    int64_t blocks = (items + kQBWarps - 1) / kQBWarps;
-    const int64_t cap = (int64_t)sm_count() * per_sm;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    err = launch_pdl(fn, dim3((unsigned)blocks), dim3(kQBWarps * 32), smem, stream, a);
-    if (err != cudaSuccess) {
-        set_cuda_error(err);
-        return MOE_ECUDA;
-    }
-    return check_launch();
-}
-} // namespace
-} // namespace moe
-#endif
-
 MOE_EXPORT int moe_dispatch_quant_fp8(const void *x, int64_t S, int64_t H, int K,
                                       const int64_t *tok_map, int block, void *packed_q,
                                       float *packed_scales, int64_t packed_rows,
@@ -1044,14 +814,9 @@ MOE_EXPORT int moe_dispatch_quant_fp8(const void *x, int64_t S, int64_t H, int K
     if (!x || !tok_map || !packed_q || !packed_scales || packed_rows < 1) return MOE_EINVAL;
     if (!aligned16(x) || !aligned16(packed_q) || (reinterpret_cast<uintptr_t>(packed_scales) & 3u))
         return MOE_EALIGN;
-    if (MOE_QUANT_WIDE && H % (4 * block) == 0 && aligned16(packed_scales))
+    if (H % (4 * block) == 0 && aligned16(packed_scales))
         return launch_quant_wide(x, S, H, K, tok_map, block, packed_q, packed_scales,
                                  packed_rows, (cudaStream_t)stream);
-#if MOE_QUANT_BULK
-    if (H % (4 * block) == 0 && aligned16(packed_scales))
-        return launch_quant_bulk(x, S, H, K, tok_map, block, packed_q, packed_scales,
-                                 packed_rows, (cudaStream_t)stream);
-#endif
     QuantArgs a = {};
     a.x = static_cast<const uint8_t *>(x);
     a.S = S;

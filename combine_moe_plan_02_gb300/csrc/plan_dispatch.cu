@@ -19,10 +19,11 @@
 // token rows (32 lanes x 16 bytes) to the token's destinations, read from
 // the CTA's own copy of the map.  No CTA waits for another CTA.
 //
-// Larger batches (up to kTiledMaxEntries) take plan_dispatch_tiles_kernel,
-// whose CTAs own token ranges instead (see there): a kernel boundary between
-// a separate plan and dispatch costs several microseconds on this part, more
-// than the redundant counting does.
+// Larger batches (up to kTiledMaxEntries entries and MOE_PD_TILED_MAX_BYTES
+// of rows) take plan_dispatch_tiles_kernel, whose CTAs own token ranges
+// instead (see there): a kernel boundary between a separate plan and dispatch
+// costs several microseconds on this part, more than the redundant counting
+// does, until the copy is long enough for the balanced dispatch to win.
 
 #include "common.cuh"
 
@@ -437,6 +438,18 @@ __global__ void __launch_bounds__(kThreads, 1) plan_dispatch_tiles_kernel(PDArgs
 #define MOE_PD_TILED 1
 #endif
 constexpr int64_t kTiledMaxEntries = 131072;
+// Copy bytes up to which the token-range kernel is used.  Its CTAs split the
+// copy statically, one range each, and SMs of this part copy at different
+// rates, so its time grows with the slowest SM's share; moe_plan followed by
+// the multi-wave moe_dispatch pays a second launch but balances the copy.
+// Measured on GB300 (plan + dispatch alone, and followed by the combine):
+// H=7168 bf16, K=8: equal at 2048 tokens (235 MB of packed rows), the two
+// calls ahead from 4096 tokens (470 MB: 89.8 against 94.0 us; with the
+// combine 175.5 against 177.5 us) and by 42 us at 16384 tokens; H=6144 fp8
+// rows with scales, K=8: the one launch ahead up to 4096 tokens (207 MB).
+#ifndef MOE_PD_TILED_MAX_BYTES
+#define MOE_PD_TILED_MAX_BYTES (384ll << 20)
+#endif
 
 int launch_tiles(const int32_t *topk_idx, const void *x, int64_t S, int K, int E,
                  int64_t row_bytes, const float *x_scales, int64_t n_scales, int32_t *cnt,
@@ -513,9 +526,12 @@ MOE_EXPORT int moe_plan_dispatch(const int32_t *topk_idx, const void *x, int64_t
     }
     const int64_t n = S * (int64_t)K;
     // larger batches: CTAs own token ranges of at most 1024 entries, one CTA
-    // per SM; each counts all n entries itself, so this stops at kTiledMax
+    // per SM; each counts all n entries itself, so this stops at kTiledMax;
+    // and above MOE_PD_TILED_MAX_BYTES of rows to copy the two calls win
     const int64_t tpc = (S + sm_count() - 1) / sm_count();
-    if (MOE_PD_TILED && n > kFusedMaxEntries && n <= kTiledMaxEntries && tpc * K <= kThreads)
+    const int64_t copy_bytes = n * (row_bytes + n_scales * 4);
+    if (MOE_PD_TILED && n > kFusedMaxEntries && n <= kTiledMaxEntries && tpc * K <= kThreads &&
+        copy_bytes <= MOE_PD_TILED_MAX_BYTES)
         return launch_tiles(topk_idx, x, S, K, E, row_bytes, x_scales, n_scales, cnt, off,
                             packed_src, tok_map, n_invalid, packed_x, packed_rows, packed_scales,
                             tpc, (cudaStream_t)stream);
