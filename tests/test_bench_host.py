@@ -82,3 +82,35 @@ def test_reference_arm_other_ranks_exit_quietly():
                         "--gpus", "2", "--steps", "1"], capture_output=True, text=True,
                        timeout=300, cwd=ROOT, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_pinned_core_restores_affinity():
+    before = os.sched_getaffinity(0)
+    with bench.PinnedCore() as pin:
+        assert os.sched_getaffinity(0) == {pin.core}
+        assert pin.core == max(before)
+    assert os.sched_getaffinity(0) == before
+
+
+def test_host_cpu_model_is_named():
+    assert isinstance(bench.host_cpu_model(), str) and bench.host_cpu_model()
+
+
+@pytest.mark.parametrize("name,S", [("tiny", None), ("dedup", 0), ("dedup", 1), ("dedup", 40),
+                                    ("fp8small", 4)])
+def test_oracle_calls_per_config(name, S):
+    """The CPU leg's per-call timing over each workload kind: every call runs
+    and reports its algorithmic bytes (the dedup workload adds the group
+    plan and the two dedup calls)."""
+    import workloads
+    wl = workloads.make(name, seed=3, S=S) if S is not None else workloads.make(name, seed=3)
+    calls = bench._oracle_calls(wl)
+    want = {"plan", "dispatch", "combine"}
+    if name == "dedup":
+        want |= {"group_plan", "dispatch_dedup", "combine_dedup"}
+    assert set(calls) == want
+    res = bench._time_calls(calls)
+    for k, v in res.items():
+        assert v["us"] > 0 and v["algorithmic_bytes"] >= 0, k
+    if S not in (0,):
+        assert res["dispatch"]["algorithmic_bytes"] > 0
