@@ -235,3 +235,22 @@ def test_bounded_wait_times_out_and_reports():
     torch.cuda.synchronize()
     ref = oracle.plan(wl.topk_idx, wl.E)
     assert np.array_equal(plan.tok_map.cpu().numpy(), ref["tok_map"])
+
+
+@pytest.mark.timeout(600)
+def test_dispatch_several_chunks_per_warp():
+    """A batch large enough that the dispatch grid (capped at a few resident
+    waves) gives warps more than one chunk, so each warp's stage is reused:
+    S=80000 rows of 4 KB, K=2.  Every packed row equals the oracle's."""
+    import combine_moe_plan_02_gb300 as moe
+    wl = workloads.make("moonep", seed=77, S=80000, H=2048, E=64, K=2)
+    d = gpu_path.to_device(wl)
+    plan = moe.moe_plan(d["topk_idx"], wl.E)
+    packed = gpu_path.poisoned((wl.S * wl.K, wl.H), torch.bfloat16)
+    moe.moe_dispatch(d["x"], plan.tok_map, packed_x=packed)
+    torch.cuda.synchronize()
+    assert moe.moe_device_errors() == 0
+    ref = oracle.plan(wl.topk_idx, wl.E)
+    assert np.array_equal(gpu_path._np(plan.tok_map), ref["tok_map"])
+    want = oracle.dispatch(wl.x, ref["tok_map"], wl.S * wl.K, fill=gpu_path.POISON)
+    assert np.array_equal(gpu_path._np(packed), want)
