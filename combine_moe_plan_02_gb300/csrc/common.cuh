@@ -82,6 +82,12 @@ cudaError_t read_dispatch_errors(uint32_t *flags);
 cudaError_t read_combine_errors(uint32_t *flags);
 cudaError_t read_plan_dispatch_errors(uint32_t *flags);
 
+// moe_dispatch's body; early_src: the source rows were complete before the
+// previous kernel of the stream started waiting (see CopyArgs::early_src).
+int dispatch_rows(const void *x, int64_t S, int64_t H, int dtype, int K, const int64_t *tok_map,
+                  void *packed_x, int64_t packed_rows, const float *x_scales, int64_t n_scales,
+                  float *packed_scales, bool early_src, cudaStream_t stream);
+
 // Number of SMs of the current device (cached per device ordinal).
 int sm_count();
 

@@ -118,6 +118,11 @@ struct CopyArgs {
     // rows read from grp_map (the group rows' expert maps)
     const int64_t *gtok_map;   // [rows, K] or null
     const int64_t *grp_map;    // [dst2_rows, K]
+    // the source rows were complete before the previous kernel of the stream
+    // started waiting for its own predecessors (the plan of moe_plan_dispatch
+    // lets its dependents launch only after that), so the first loads may be
+    // issued before this kernel waits; with src_map or rows_dev: ignored
+    bool early_src;
 };
 
 __global__ void __launch_bounds__(kWarpsPerCta * 32) dispatch_bulk_kernel(CopyArgs a)
@@ -135,8 +140,14 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) dispatch_bulk_kernel(CopyAr
     }
     __syncwarp();
 
-    griddep_wait();  // earlier stream work (the plan; readers of packed_x) is done
-    griddep_launch_dependents();
+    // Everything that reads the maps or writes packed rows waits for earlier
+    // stream work (the plan; readers of packed_x).  With early_src the first
+    // source loads go out before that wait, while the plan finishes.
+    const bool early = a.early_src && a.src_map == nullptr && a.rows_dev == nullptr;
+    if (!early) {
+        griddep_wait();
+        griddep_launch_dependents();
+    }
 
     const int64_t rows = a.rows_dev ? min(*a.rows_dev, a.rows) : a.rows;
     const int64_t n_items = rows * a.n_chunks;
@@ -149,7 +160,9 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) dispatch_bulk_kernel(CopyAr
     int64_t dst_row[kStages];  // this lane's destination row per stage
     int64_t issued = 0;        // items whose load has been issued
 
-    auto issue = [&](int64_t j, int st) {
+    // the source chunk of item j into stage st; returns whether the source
+    // row lies inside its buffer
+    auto issue_load = [&](int64_t j, int st) -> bool {
         issued = j + 1;
         const int64_t it = gw + j * W;
         const int64_t r = it / a.n_chunks;
@@ -174,6 +187,13 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) dispatch_bulk_kernel(CopyAr
                 atomicOr(&g_dispatch_error, kErrDispatchIndex);
             }
         }
+        return src_ok;
+    };
+
+    // this lane's destination row of item j, from the maps
+    auto issue_dst = [&](int64_t j, int st, bool src_ok) {
+        const int64_t it = gw + j * W;
+        const int64_t r = it / a.n_chunks;
         int64_t d = -1;
         bool second;  // this lane stores to dst2
         if (a.gtok_map) {
@@ -214,10 +234,24 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) dispatch_bulk_kernel(CopyAr
         dst_row[st] = d;
     };
 
+    auto issue = [&](int64_t j, int st) { issue_dst(j, st, issue_load(j, st)); };
+
     // prologue: fill the ring
+    if (early) {
+        bool ok_src[kStages];
 #pragma unroll
-    for (int st = 0; st < kStages; ++st)
-        if (st < n_mine) issue(st, st);
+        for (int st = 0; st < kStages; ++st)
+            if (st < n_mine) ok_src[st] = issue_load(st, st);
+        griddep_wait();
+        griddep_launch_dependents();
+#pragma unroll
+        for (int st = 0; st < kStages; ++st)
+            if (st < n_mine) issue_dst(st, st, ok_src[st]);
+    } else {
+#pragma unroll
+        for (int st = 0; st < kStages; ++st)
+            if (st < n_mine) issue(st, st);
+    }
 
     bool ok = true;
     int64_t consumed = 0;   // items whose load has been waited for
@@ -666,6 +700,17 @@ MOE_EXPORT int moe_dispatch(const void *x, int64_t S, int64_t H, int dtype, int 
                             moe_stream_t stream)
 {
     MOE_TRACE("moe_dispatch");
+    return dispatch_rows(x, S, H, dtype, K, tok_map, packed_x, packed_rows, x_scales, n_scales,
+                         packed_scales, false, (cudaStream_t)stream);
+}
+
+// moe_dispatch; with early_src (moe_plan_dispatch, right after its plan) the
+// first source loads may precede the wait for the plan
+int moe::dispatch_rows(const void *x, int64_t S, int64_t H, int dtype, int K,
+                       const int64_t *tok_map, void *packed_x, int64_t packed_rows,
+                       const float *x_scales, int64_t n_scales, float *packed_scales,
+                       bool early_src, cudaStream_t stream)
+{
     const int es = elem_size(dtype);
     if (es == 0 || S < 0 || H < 1 || K < 1 || K > 32 || n_scales < 0) return MOE_EINVAL;
     if (S == 0) return MOE_OK;
@@ -690,7 +735,8 @@ MOE_EXPORT int moe_dispatch(const void *x, int64_t S, int64_t H, int dtype, int 
     a.ssrc = reinterpret_cast<const uint8_t *>(x_scales);
     a.sdst = reinterpret_cast<uint8_t *>(packed_scales);
     a.scale_bytes = (int)(n_scales * 4);
-    return launch_copy(a, (cudaStream_t)stream);
+    a.early_src = early_src;
+    return launch_copy(a, stream);
 }
 
 MOE_EXPORT int moe_dispatch_dedup(const void *x, int64_t S, int64_t H, int dtype, int K, int G,

@@ -478,12 +478,16 @@ __global__ void __launch_bounds__(kThreads, 1) plan_rank_kernel(Key key, int nke
     const int t = blockIdx.x;
     const bool single = (g.mode == kModeSingle);
 
-    griddep_launch_dependents();
     // Unless kernel 1 ran first, nothing of this plan ran before: wait for
-    // whatever wrote topk_idx.  In two-kernel mode kernel 1 was launched
-    // without the attribute, so it (and this kernel) began only after earlier
-    // stream work finished, and topk_idx may be read before the wait.
+    // whatever wrote topk_idx, and only then let the next kernel launch, so
+    // that everything before this plan is complete when the next kernel
+    // starts (the dispatch of moe_plan_dispatch loads x before its own wait).
+    // In two-kernel mode kernel 1 was launched without the attribute, so it
+    // (and this kernel) began only after earlier stream work finished:
+    // topk_idx may be read before the wait, and the dependents may launch at
+    // once.
     if (g.mode != kModeTwoKernel) griddep_wait();
+    griddep_launch_dependents();
 
     const int64_t wbegin = (int64_t)t * g.tile + (int64_t)warp * g.sub;
     const int64_t wend = min(wbegin + g.sub, g.n);

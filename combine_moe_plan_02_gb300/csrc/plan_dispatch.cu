@@ -536,12 +536,14 @@ MOE_EXPORT int moe_plan_dispatch(const int32_t *topk_idx, const void *x, int64_t
                             packed_src, tok_map, n_invalid, packed_x, packed_rows, packed_scales,
                             tpc, (cudaStream_t)stream);
     if (n == 0 || n > kFusedMaxEntries) {
-        // throughput path: the two calls it fuses, back to back
+        // throughput path: the two calls it fuses, back to back; the plan's
+        // kernel lets the dispatch launch only once everything before the
+        // plan is complete, so the dispatch may load x before it waits
         if (int rc = moe_plan(topk_idx, S, K, E, cnt, off, packed_src, tok_map, n_invalid,
                               workspace, workspace_bytes, stream))
             return rc;
-        return moe_dispatch(x, S, H, dtype, K, tok_map, packed_x, packed_rows, x_scales,
-                            n_scales, packed_scales, stream);
+        return dispatch_rows(x, S, H, dtype, K, tok_map, packed_x, packed_rows, x_scales,
+                             n_scales, packed_scales, true, (cudaStream_t)stream);
     }
     PDArgs a = {};
     a.idx = topk_idx;
