@@ -709,10 +709,10 @@ def run_ours(args):
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
     # the rule moe_plan_dispatch applies: one launch up to 1024 entries, or
     # up to 131072 entries with at most 1024 per SM's token range and at most
-    # 384 MiB of rows to copy; else moe_plan then moe_dispatch
+    # 192 MiB of rows to copy; else moe_plan then moe_dispatch
     one_launch = (S * K <= int(moe.lib().moe_plan_dispatch_fused_max())
                   or (S * K <= 131072 and -(-S // n_sm) * K <= 1024
-                      and S * K * H * 2 <= (384 << 20)))
+                      and S * K * H * 2 <= (192 << 20)))
     launches_per_step = (1 if one_launch else
                          (2 if moe.moe_plan_workspace_size(S, K, E) > 0 else 1) + 1) + 1
 

@@ -441,14 +441,15 @@ constexpr int64_t kTiledMaxEntries = 131072;
 // Copy bytes up to which the token-range kernel is used.  Its CTAs split the
 // copy statically, one range each, and SMs of this part copy at different
 // rates, so its time grows with the slowest SM's share; moe_plan followed by
-// the multi-wave moe_dispatch pays a second launch but balances the copy.
-// Measured on GB300 (plan + dispatch alone, and followed by the combine):
-// H=7168 bf16, K=8: equal at 2048 tokens (235 MB of packed rows), the two
-// calls ahead from 4096 tokens (470 MB: 89.8 against 94.0 us; with the
-// combine 175.5 against 177.5 us) and by 42 us at 16384 tokens; H=6144 fp8
-// rows with scales, K=8: the one launch ahead up to 4096 tokens (207 MB).
+// the multi-wave dispatch pays a second launch but balances the copy (and
+// overlaps its first loads with the plan).  Measured on GB300 (plan +
+// dispatch alone, and followed by the combine): H=7168 bf16, K=8: the one
+// launch ahead at 1536 tokens (176 MB of packed rows: 37.3 against 40.1 us),
+// the two calls ahead from 2048 tokens (235 MB: 48.8 against 50.8 us; with
+// the combine 87.2 against 90.3 us) and by 2-40 us beyond; H=6144 fp8 rows
+// with scales, K=8: the one launch ahead or level up to 4096 tokens (207 MB).
 #ifndef MOE_PD_TILED_MAX_BYTES
-#define MOE_PD_TILED_MAX_BYTES (384ll << 20)
+#define MOE_PD_TILED_MAX_BYTES (192ll << 20)
 #endif
 
 int launch_tiles(const int32_t *topk_idx, const void *x, int64_t S, int K, int E,

@@ -266,7 +266,7 @@ int moe_dispatch_quant_fp8(const void *x, int64_t S, int64_t H, int K,
  * the same arguments, layouts and rules as those two calls.  One kernel does
  * both when 0 < S*K <= moe_plan_dispatch_fused_max() (every CTA ranks all
  * entries in shared memory) and when S*K <= 131072 with at most 1024 entries
- * per SM's share of the tokens and at most 384 MiB of rows to copy (each CTA
+ * per SM's share of the tokens and at most 192 MiB of rows to copy (each CTA
  * owns a token range: it counts all entries, ranks its own and copies its
  * own rows); the workspace is then not used.  Otherwise the call enqueues
  * moe_plan then moe_dispatch (whose grid balances the copy across SMs), and

@@ -84,13 +84,14 @@ def test_bf16_shapes(S, H, E, K):
     _check(workloads.make("moonep", seed=S + E, S=S, H=H, E=E, K=K))
 
 
-@pytest.mark.parametrize("S,H,E,K", [(2048, 7168, 64, 8), (4096, 7168, 64, 8), (3000, 264, 1024, 32),
-                                     (5000, 136, 37, 5), (16000, 16, 64, 8), (200, 6144, 256, 8)])
+@pytest.mark.parametrize("S,H,E,K", [(1536, 7168, 64, 8), (2048, 7168, 64, 8), (4096, 7168, 64, 8),
+                                     (3000, 264, 1024, 32), (5000, 136, 37, 5), (16000, 16, 64, 8),
+                                     (200, 6144, 256, 8)])
 def test_tiled_one_launch_shapes(S, H, E, K):
-    """Above 1024 entries and up to 131072 entries and 384 MiB of rows, one
-    launch whose CTAs own token ranges (2048 x 7168 is near the byte limit);
-    the benchmark shape (4096 x 7168, 470 MB of rows) takes plan then
-    dispatch; 19456 x 8 would exceed the entry range."""
+    """Above 1024 entries and up to 131072 entries and 192 MiB of rows, one
+    launch whose CTAs own token ranges (1536 x 7168 is near the byte limit);
+    2048 x 7168 and the benchmark shape (4096 x 7168, 470 MB of rows) take
+    plan then dispatch; 19456 x 8 would exceed the entry range."""
     _check(workloads.make("moonep", seed=S + K, S=S, H=H, E=E, K=K))
 
 
