@@ -158,14 +158,18 @@ def test_empty_batch():
     assert plan.cnt.sum().item() == 0 and plan.off.sum().item() == 0
 
 
-@pytest.mark.parametrize("S", [16, 600])
-def test_cuda_graph_replay(S):
-    """Plan, dispatch and combine captured once into a CUDA graph (one fused
-    launch at 16 tokens, two calls at 600) and replayed on new inputs copied
-    into the captured buffers: every replay matches the oracle."""
+@pytest.mark.timeout(900)
+@pytest.mark.parametrize("S,H", [(16, 1032), (600, 1032), (4096, 3200), (20000, 16)])
+def test_cuda_graph_replay(S, H):
+    """Plan, dispatch and combine captured once into a CUDA graph and
+    replayed on new inputs copied into the captured buffers, for every form
+    of moe_plan_dispatch: one fused launch (16 tokens), the token-range
+    launch (600), plan then dispatch with the dispatch's early loads (4096 x
+    3200: 210 MB of rows), and the two-kernel plan then dispatch (20000
+    tokens); every replay matches the oracle."""
     import combine_moe_plan_02_gb300 as moe
     dev = torch.device("cuda")
-    wls = [workloads.make("moonep", seed=80 + r, S=S, H=1032, E=64, K=8) for r in range(3)]
+    wls = [workloads.make("moonep", seed=80 + r, S=S, H=H, E=64, K=8) for r in range(3)]
     wl = wls[0]
     idx = torch.from_numpy(wl.topk_idx).to(dev)
     w = torch.from_numpy(wl.topk_w).to(dev)
