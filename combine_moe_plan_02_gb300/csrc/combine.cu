@@ -167,11 +167,11 @@ template <> struct Io<float> {
 };
 
 // Register budgets are set as resident threads per SM, whatever the CTA
-// size: 512 for the general and dedup kernels (<= 128 registers), 768 for
-// the lean one (<= 85).  128-thread CTAs fit more warps per SM than 256-thread
-// ones at the same budget (seven lean CTAs = 28 warps at 72 registers,
-// against three of 256 = 24): the combine at the MoonEP shape went 77.8 ->
-// 75.7 us alone and 90.2 -> 89.3 us inside the step.
+// size: 512 for the general and dedup kernels (<= 128 registers), 640 for
+// the lean one (<= 102).  128-thread CTAs fit more warps per SM than
+// 256-thread ones at the same budget: the combine at the MoonEP shape went
+// 77.8 -> 75.7 us alone and 90.2 -> 89.3 us inside the step with seven lean
+// CTAs of 72 registers (28 warps) against three of 256 threads.
 #ifndef MOE_COMBINE_MIN_BLOCKS
 #define MOE_COMBINE_MIN_BLOCKS (512 / MOE_COMBINE_THREADS)
 #endif
@@ -272,22 +272,25 @@ __global__ void __launch_bounds__(kThreads, MOE_COMBINE_MIN_BLOCKS) combine_kern
 
 // ---------------------------------------------------------------------------
 // The same sum for the common case -- bf16 rows in and out, weights per
-// output row or none, K <= 8, with or without the weight fold -- written to
-// hold fewer registers so that more warps fit on an SM and more gathers are
-// in flight: per unit the lanes keep one row pointer each (shuffled to the
-// warp when a step issues its loads) and one ballot of the valid entries
-// instead of K row indices, and each 32-bit word of a gathered vector is
-// widened and added in place.  At 72 registers 24 to 28 warps fit per SM
-// instead of 16, and the combine of 4096 rows of 7168 bf16 from K = 8
-// gathered rows drops from 90 to 75 us.  The order of operations is the
-// kernel's above, for every mode.
+// output row or none, K <= 8, with or without the weight fold -- written so
+// that more gathers are in flight per SM: per unit the lanes keep one row
+// pointer each (shuffled to the warp when a step issues its loads) and one
+// ballot of the valid entries instead of K row indices, and each 32-bit word
+// of a gathered vector is widened and added in place.  A lane gathers two
+// steps at once (2 x K 16-byte loads in flight before the first add), which
+// costs 96 registers; five 128-thread CTAs (20 warps) then hold 160 KB of
+// gathers per SM, against 112 KB for one step at a time with 28 warps of 72
+// registers.  The combine of 4096 rows of 7168 bf16 from K = 8 gathered
+// rows: 90 us on the general kernel, 75.5 us one step at a time, 71.9 us
+// two steps at a time (85.0 against 89.1 us inside the step).  The order of
+// operations on every element is the kernel's above, for every mode.
 // ---------------------------------------------------------------------------
 
 #ifndef MOE_COMBINE_LEAN
 #define MOE_COMBINE_LEAN 1
 #endif
 #ifndef MOE_COMBINE_LEAN_MIN_BLOCKS
-#define MOE_COMBINE_LEAN_MIN_BLOCKS (768 / MOE_COMBINE_THREADS)
+#define MOE_COMBINE_LEAN_MIN_BLOCKS (640 / MOE_COMBINE_THREADS)
 #endif
 
 template <bool kWeighted, bool kFold>
@@ -331,39 +334,49 @@ combine_lean_kernel(CombineArgs a)
         }
         const int64_t pbase = (int64_t)sl * 32 * a.R;
         uint8_t *out_row = a.out + i * row_bytes;
-        for (int r = 0; r < a.R; ++r) {
-            const int64_t p = pbase + (int64_t)r * 32 + lane;
-            const bool active = p < a.steps;
-            uint4 v[kKChunk];
+        for (int r = 0; r < a.R; r += 2) {
+            const int64_t p0 = pbase + (int64_t)r * 32 + lane;
+            const int64_t p1 = p0 + 32;
+            const bool act0 = p0 < a.steps;
+            const bool act1 = r + 1 < a.R && p1 < a.steps;
+            uint4 v0[kKChunk], v1[kKChunk];
 #pragma unroll
             for (int k = 0; k < kKChunk; ++k) {
                 const uint8_t *bk = reinterpret_cast<const uint8_t *>(
                     __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(base), k));
-                if (active && ((vmask >> k) & 1u)) v[k] = ld_stream16(bk + p * 16);
+                if ((vmask >> k) & 1u) {
+                    if (act0) v0[k] = ld_stream16(bk + p0 * 16);
+                    if (act1) v1[k] = ld_stream16(bk + p1 * 16);
+                }
             }
-            float acc[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+            for (int h = 0; h < 2; ++h) {
+                const bool active = h ? act1 : act0;
+                float acc[8];
 #pragma unroll
-            for (int k = 0; k < kKChunk; ++k) {
-                const float wk = kWeighted ? __shfl_sync(0xffffffffu, w, k) : 1.0f;
-                if (active && ((vmask >> k) & 1u)) {
-                    const uint32_t q[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+                for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float lo = __uint_as_float(q[e] << 16);
-                        const float hi = __uint_as_float(q[e] & 0xffff0000u);
-                        if (kWeighted) {
-                            acc[2 * e] = __fadd_rn(acc[2 * e], __fmul_rn(wk, lo));
-                            acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], __fmul_rn(wk, hi));
-                        } else {
-                            acc[2 * e] = __fadd_rn(acc[2 * e], lo);
-                            acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], hi);
+                for (int k = 0; k < kKChunk; ++k) {
+                    const float wk = kWeighted ? __shfl_sync(0xffffffffu, w, k) : 1.0f;
+                    if (active && ((vmask >> k) & 1u)) {
+                        const uint4 vk = h ? v1[k] : v0[k];
+                        const uint32_t q[4] = {vk.x, vk.y, vk.z, vk.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float lo = __uint_as_float(q[e] << 16);
+                            const float hi = __uint_as_float(q[e] & 0xffff0000u);
+                            if (kWeighted) {
+                                acc[2 * e] = __fadd_rn(acc[2 * e], __fmul_rn(wk, lo));
+                                acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], __fmul_rn(wk, hi));
+                            } else {
+                                acc[2 * e] = __fadd_rn(acc[2 * e], lo);
+                                acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], hi);
+                            }
                         }
                     }
                 }
+                if (active) Io<__nv_bfloat16>::store(out_row, h ? p1 : p0, acc, false);
             }
-            if (active) Io<__nv_bfloat16>::store(out_row, p, acc, false);
         }
     }
 }
