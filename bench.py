@@ -878,7 +878,8 @@ def run_ours(args):
         m = statistics.mean(ts)
         gbs = nb / (m / 1e3) / 1e9
         return {"us": round(1e3 * m, 2), "us_median": round(1e3 * statistics.median(ts), 2),
-                "us_min": round(1e3 * min(ts), 2), "GB_per_s": round(gbs, 1),
+                "us_min": round(1e3 * min(ts), 2), "us_std": round(1e3 * statistics.pstdev(ts), 2),
+                "GB_per_s": round(gbs, 1),
                 "frac_of_peak": round(gbs / peak, 4), "frac_of_spec": round(gbs / SPEC_HBM_GBS, 4),
                 "algorithmic_bytes": nb}
 
