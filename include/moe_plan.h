@@ -201,6 +201,13 @@ int moe_plan_static_scratch(const int32_t *topk_idx, int64_t S, int K, int E,
  * gcnt         int32 [G]; goff int64 [G + 1]; gtok_map int64 [S, K]
  * grp_src      int32 [S * min(K, G)]        first R entries written
  * grp_tok_map  int64 [S * min(K, G), K]     first R rows written
+ * workspace    moe_group_plan_workspace_size(S, K, E, group_size) bytes of
+ *              device scratch, 256-byte aligned, contents dead after the
+ *              call: the per-tile counts of a first kernel, so that each
+ *              tile is counted once.  Up to 131072 entries S*K it may be NULL
+ *              (or smaller); the plan then runs in one launch whose CTAs
+ *              count all entries themselves, which is slower (26.6 against
+ *              12.3 us at S=4096, K=8, 8 groups).
  * Limits: as moe_plan; group_size >= 1 divides E.
  * ---------------------------------------------------------------------- */
 size_t moe_group_plan_workspace_size(int64_t S, int K, int E, int group_size);

@@ -42,6 +42,9 @@ def test_plan_workspace_size(L):
     assert ws > 0 and ws % 256 == 0
     assert L.moe_plan_workspace_size(20000, 0, 64) == 0         # invalid K
     assert L.moe_group_plan_workspace_size(20000, 8, 64, 8) > 0
+    assert L.moe_group_plan_workspace_size(128, 8, 64, 8) == 0     # one tile: no scratch
+    gws = L.moe_group_plan_workspace_size(4096, 8, 64, 8)          # tiles counted once
+    assert gws > 0 and gws % 256 == 0
     assert L.moe_group_plan_workspace_size(4096, 8, 64, 7) == 0  # 7 does not divide 64
 
 

@@ -254,3 +254,40 @@ def test_dispatch_several_chunks_per_warp():
     assert np.array_equal(gpu_path._np(plan.tok_map), ref["tok_map"])
     want = oracle.dispatch(wl.x, ref["tok_map"], wl.S * wl.K, fill=gpu_path.POISON)
     assert np.array_equal(gpu_path._np(packed), want)
+
+
+@pytest.mark.timeout(600)
+@pytest.mark.parametrize("S,E,gs,K", [(4096, 64, 8, 8), (3000, 256, 4, 6), (16384, 64, 2, 8)])
+def test_group_plan_with_and_without_workspace(S, E, gs, K):
+    """The group plan counts each tile once when given its workspace (two
+    kernels) and lets every CTA count all entries without it (one launch):
+    both give the oracle's group plan."""
+    import combine_moe_plan_02_gb300 as moe
+    L = moe.lib()
+    wl = workloads.make("moonep", seed=S + gs, S=S, H=8, E=E, K=K)
+    dev = torch.device("cuda")
+    idx = torch.from_numpy(wl.topk_idx).to(dev)
+    plan = moe.moe_plan(idx, E)
+    G = E // gs
+    rmax = S * min(K, G)
+    need = int(L.moe_group_plan_workspace_size(S, K, E, gs))
+    assert need > 0
+    ref = oracle.group_plan(wl.topk_idx, oracle.plan(wl.topk_idx, E)["tok_map"], E, gs)
+    R = int(ref["goff"][-1])
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    for ptr, nbytes in ((ws.data_ptr(), need), (None, 0)):
+        out = [gpu_path.poisoned((G,), torch.int32), gpu_path.poisoned((G + 1,), torch.int64),
+               gpu_path.poisoned((S, K), torch.int64), gpu_path.poisoned((rmax,), torch.int32),
+               gpu_path.poisoned((rmax, K), torch.int64)]
+        rc = L.moe_group_plan(idx.data_ptr(), plan.tok_map.data_ptr(), S, K, E, gs,
+                              *[t.data_ptr() for t in out], ptr, nbytes,
+                              torch.cuda.current_stream().cuda_stream)
+        assert rc == 0, L.moe_status_string(rc)
+        torch.cuda.synchronize()
+        np_ = gpu_path._np
+        assert np.array_equal(np_(out[0]), ref["gcnt"])
+        assert np.array_equal(np_(out[1]), ref["goff"])
+        assert np.array_equal(np_(out[2]), ref["gtok_map"])
+        assert np.array_equal(np_(out[3])[:R], ref["grp_src"])
+        assert np.array_equal(np_(out[4])[:R], ref["grp_tok_map"])
+    assert moe.moe_device_errors() == 0
