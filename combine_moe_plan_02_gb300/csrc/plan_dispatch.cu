@@ -37,6 +37,13 @@ constexpr int kSeg = 512;       // bytes of a row segment copied by one warp
 #define MOE_PLAN_DISPATCH_FUSED_MAX 1024
 #endif
 constexpr int64_t kFusedMaxEntries = MOE_PLAN_DISPATCH_FUSED_MAX;
+// 256-thread CTAs when E <= 256: a quarter of the count table to clear and
+// scan (fp8 rows, H=6144 E=256 K=8, per call back to back in a graph: 6.54 ->
+// 4.57 us at 4..16 tokens, 8.60 -> 7.58 us at 128, 12.93 at 1024 either way;
+// two or four such CTAs per SM made 128 tokens slower, 9.2 us)
+#ifndef MOE_PD_NARROW
+#define MOE_PD_NARROW 1
+#endif
 
 __device__ uint32_t g_pd_error;  // kErrDispatchIndex
 
@@ -60,7 +67,8 @@ struct PDArgs {
     int64_t packed_rows;
 };
 
-// Exclusive scan of v over the block; sets `total`.
+// Exclusive scan of v over a block of kW warps; sets `total`.
+template <int kW = kWarps>
 __device__ __forceinline__ int32_t block_scan(int32_t v, int32_t *s_warp, int32_t &total)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -72,15 +80,15 @@ __device__ __forceinline__ int32_t block_scan(int32_t v, int32_t *s_warp, int32_
     if (lane == 31) s_warp[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        int32_t w = s_warp[lane];
+        int32_t w = lane < kW ? s_warp[lane] : 0;
         for (int o = 1; o < 32; o <<= 1) {
             const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
             if (lane >= o) w += y;
         }
-        s_warp[lane] = w;
+        if (lane < kW) s_warp[lane] = w;
     }
     __syncthreads();
-    total = s_warp[kWarps - 1];
+    total = s_warp[kW - 1];
     return (warp ? s_warp[warp - 1] : 0) + x - v;
 }
 
@@ -92,14 +100,18 @@ __device__ __forceinline__ int entry_key(const PDArgs &a, int64_t i, bool in_ran
     return (e >= 0 && e < a.E) ? e : -1;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) plan_dispatch_kernel(PDArgs a)
+// kT threads per CTA: 1024, or 256 when E <= 256 (a smaller count table to
+// clear and scan for the same ranks).
+template <int kT>
+__global__ void __launch_bounds__(kT, 1) plan_dispatch_kernel(PDArgs a)
 {
+    constexpr int kW = kT / 32;
     extern __shared__ int32_t smem[];
     const int wstride = a.E | 1;                 // odd: the column walks hit 32 banks
-    int32_t *s_wc = smem;                        // [kWarps][wstride] per-warp counts
-    int32_t *s_off = s_wc + kWarps * wstride;    // [E] bucket offsets
+    int32_t *s_wc = smem;                        // [kW][wstride] per-warp counts
+    int32_t *s_off = s_wc + kW * wstride;        // [E] bucket offsets
     int32_t *s_row = s_off + a.E;                // [n] packed row of each entry
-    __shared__ int32_t s_scan[kWarps];
+    __shared__ int32_t s_scan[kW];
     __shared__ int32_t s_inval;
 
     griddep_wait();  // topk_idx and x come from earlier stream work
@@ -112,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1) plan_dispatch_kernel(PDArgs a)
     // first (token, segment) unit now, so that the load overlaps the ranking.
     const int64_t per_tok = a.segs + a.ssegs;
     const int64_t units = a.S * per_tok;
-    const int64_t u0 = (int64_t)blockIdx.x * kWarps + warp;
+    const int64_t u0 = (int64_t)blockIdx.x * kW + warp;
     uint4 v0 = make_uint4(0, 0, 0, 0);
     {
         const int64_t s = u0 / per_tok;
@@ -123,12 +135,12 @@ __global__ void __launch_bounds__(kThreads, 1) plan_dispatch_kernel(PDArgs a)
         if (u0 < units && ob < len) v0 = ld_stream16((is_row ? a.x : a.xs) + s * len + ob);
     }
 
-    for (int i = threadIdx.x; i < kWarps * wstride; i += kThreads) s_wc[i] = 0;
+    for (int i = threadIdx.x; i < kW * wstride; i += kT) s_wc[i] = 0;
     if (threadIdx.x == 0) s_inval = 0;
     __syncthreads();
 
     // each warp owns `sub` consecutive entries (a multiple of 32)
-    const int64_t sub = (a.n + kThreads - 1) / kThreads * 32;
+    const int64_t sub = (a.n + kT - 1) / kT * 32;
     const int64_t wbegin = (int64_t)warp * sub;
     const int64_t wend = min(wbegin + sub, a.n);
     int32_t *my_wc = s_wc + warp * wstride;
@@ -151,9 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1) plan_dispatch_kernel(PDArgs a)
     const int e = threadIdx.x;
     int32_t tot = 0;
     if (e < a.E)
-        for (int w = 0; w < kWarps; ++w) tot += s_wc[w * wstride + e];
+        for (int w = 0; w < kW; ++w) tot += s_wc[w * wstride + e];
     int32_t total;
-    const int32_t offe = block_scan(tot, s_scan, total);
+    const int32_t offe = block_scan<kW>(tot, s_scan, total);
     if (e < a.E) {
         s_off[e] = offe;
         if (writer) {
@@ -167,14 +179,14 @@ __global__ void __launch_bounds__(kThreads, 1) plan_dispatch_kernel(PDArgs a)
     }
 
     // per expert, exclusive scan over the warps (lane l holds warp l)
-    for (int k = warp; k < a.E; k += kWarps) {
-        const int32_t c = s_wc[lane * wstride + k];
+    for (int k = warp; k < a.E; k += kW) {
+        const int32_t c = lane < kW ? s_wc[lane * wstride + k] : 0;
         int32_t x = c;
-        for (int sh = 1; sh < 32; sh <<= 1) {
+        for (int sh = 1; sh < kW; sh <<= 1) {
             const int32_t y = __shfl_up_sync(0xffffffffu, x, sh);
             if (lane >= sh) x += y;
         }
-        s_wc[lane * wstride + k] = x - c;
+        if (lane < kW) s_wc[lane * wstride + k] = x - c;
     }
     __syncthreads();
 
@@ -200,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) plan_dispatch_kernel(PDArgs a)
     __syncthreads();
 
     // rows: unit = (token, segment); scale rows follow the row's segments
-    for (int64_t u = u0; u < units; u += (int64_t)gridDim.x * kWarps) {
+    for (int64_t u = u0; u < units; u += (int64_t)gridDim.x * kW) {
         const int64_t s = u / per_tok;
         const int64_t g = u - s * per_tok;
         const bool is_row = g < a.segs;
@@ -567,21 +579,24 @@ MOE_EXPORT int moe_plan_dispatch(const int32_t *topk_idx, const void *x, int64_t
     a.ps = reinterpret_cast<uint8_t *>(packed_scales);
     a.packed_rows = packed_rows;
 
-    const size_t smem = ((size_t)kWarps * (E | 1) + (size_t)E + (size_t)n) * sizeof(int32_t);
-    static KernelCache cache;
+    // one warp per (token, segment) unit, at most one CTA per SM
+    const bool narrow = MOE_PD_NARROW && E <= 256;
+    const int threads = narrow ? 256 : kThreads;
+    void (*fn)(PDArgs) = narrow ? plan_dispatch_kernel<256> : plan_dispatch_kernel<kThreads>;
+    const size_t smem =
+        ((size_t)(threads / 32) * (E | 1) + (size_t)E + (size_t)n) * sizeof(int32_t);
+    static KernelCache caches[2];
     int per_sm = 0;
-    cudaError_t err = prepare_kernel(plan_dispatch_kernel, smem, kThreads, cache, &per_sm);
+    cudaError_t err = prepare_kernel(fn, smem, threads, caches[narrow], &per_sm);
     if (err != cudaSuccess || per_sm < 1) {
         set_cuda_error(err != cudaSuccess ? err : cudaErrorInvalidConfiguration);
         return MOE_ECUDA;
     }
-    // one warp per (token, segment) unit, at most one CTA per SM
     const int64_t units = S * (a.segs + a.ssegs);
-    int64_t blocks = (units + kWarps - 1) / kWarps;
+    int64_t blocks = (units + threads / 32 - 1) / (threads / 32);
     if (blocks > sm_count()) blocks = sm_count();
     if (blocks < 1) blocks = 1;
-    err = launch_pdl(plan_dispatch_kernel, dim3((unsigned)blocks), dim3(kThreads), smem,
-                     (cudaStream_t)stream, a);
+    err = launch_pdl(fn, dim3((unsigned)blocks), dim3(threads), smem, (cudaStream_t)stream, a);
     if (err != cudaSuccess) {
         set_cuda_error(err);
         return MOE_ECUDA;
