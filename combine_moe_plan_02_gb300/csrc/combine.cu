@@ -167,8 +167,8 @@ template <> struct Io<float> {
 };
 
 // Register budgets are set as resident threads per SM, whatever the CTA
-// size: 512 for the general and dedup kernels (<= 128 registers), 640 for
-// the lean one (<= 102).  128-thread CTAs fit more warps per SM than
+// size: 512 for the general kernel (<= 128 registers), 640 for the lean one
+// (<= 102); the dedup kernel's are set by input type, below.  128-thread CTAs fit more warps per SM than
 // 256-thread ones at the same budget: the combine at the MoonEP shape went
 // 77.8 -> 75.7 us alone and 90.2 -> 89.3 us inside the step with seven lean
 // CTAs of 72 registers (28 warps) against three of 256 threads.
@@ -410,8 +410,23 @@ struct DedupArgs {
     uint8_t *out;              // [S, H]
 };
 
+// Register budgets of the dedup kernel as resident threads per SM, by input
+// type.  Each entry's row, representative and weight stay in its lane and
+// are shuffled out where used instead of being held per lane for all K
+// entries (117 -> 96 registers with f32 rows, 121 -> 72 with bf16 rows): at
+// S=4096 K=8 in 8 groups, f32 rows of 4096 154.5 -> 153.3 us (five CTAs per
+// SM; six spill, 171.7 us), bf16 rows of 7168 with f32 group rows 207.6 ->
+// 178.5 us (six or seven CTAs per SM, 72 registers either way).
+#ifndef MOE_DEDUP_THREADS_F32
+#define MOE_DEDUP_THREADS_F32 640
+#endif
+#ifndef MOE_DEDUP_THREADS_BF16
+#define MOE_DEDUP_THREADS_BF16 768
+#endif
+
 template <typename Tin, typename Tout>
-__global__ void __launch_bounds__(kThreads, MOE_COMBINE_MIN_BLOCKS)
+__global__ void __launch_bounds__(kThreads, (sizeof(Tin) == 4 ? MOE_DEDUP_THREADS_F32
+                                                               : MOE_DEDUP_THREADS_BF16) / kThreads)
 combine_dedup_kernel(DedupArgs a)
 {
     griddep_wait();
@@ -462,13 +477,13 @@ combine_dedup_kernel(DedupArgs a)
             }
         }
         const float my_w = (lane < K && my_row >= 0) ? __ldg(a.w + s * K + lane) : 0.0f;
-        int32_t rk[kKChunk], jk[kKChunk];
-        float wk[kKChunk];
+        // entry k's representative rank in nibble k (15: entry unused); its
+        // row and weight stay in lane k and are shuffled out where used
+        uint32_t jmask = 0;
 #pragma unroll
         for (int kk = 0; kk < kKChunk; ++kk) {
-            rk[kk] = __shfl_sync(0xffffffffu, my_row, kk);
-            jk[kk] = __shfl_sync(0xffffffffu, my_rep, kk);
-            wk[kk] = __shfl_sync(0xffffffffu, my_w, kk);
+            const int j = __shfl_sync(0xffffffffu, my_rep, kk);
+            jmask |= (uint32_t)((kk < K && j >= 0) ? j : 15) << (4 * kk);
         }
         const int n_reps = __popc(reps);
         const int64_t pbase = (int64_t)sl * 32 * a.R;
@@ -480,9 +495,11 @@ combine_dedup_kernel(DedupArgs a)
             const bool quad = kQuad && (((p >> 5) + 1) << 5) <= a.steps;
             uint4 v[kKChunk][Io<Tin>::kVec];
 #pragma unroll
-            for (int kk = 0; kk < kKChunk; ++kk)
-                if (active && kk < K && rk[kk] >= 0)
-                    Io<Tin>::load(v[kk], a.y + (int64_t)rk[kk] * in_row_bytes, p, quad);
+            for (int kk = 0; kk < kKChunk; ++kk) {
+                const int32_t rr = __shfl_sync(0xffffffffu, my_row, kk);
+                if (active && ((jmask >> (4 * kk)) & 15u) != 15u)
+                    Io<Tin>::load(v[kk], a.y + (int64_t)rr * in_row_bytes, p, quad);
+            }
             float tot[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) tot[q] = 0.0f;
@@ -494,11 +511,14 @@ combine_dedup_kernel(DedupArgs a)
                 for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
 #pragma unroll
                 for (int kk = 0; kk < kKChunk; ++kk) {
-                    if (active && kk < K && rk[kk] >= 0 && jk[kk] == j) {
-                        float f[8];
-                        Io<Tin>::widen(v[kk], f);
+                    if (((jmask >> (4 * kk)) & 15u) == (uint32_t)j) {  // warp-uniform
+                        const float wk = __shfl_sync(0xffffffffu, my_w, kk);
+                        if (active) {
+                            float f[8];
+                            Io<Tin>::widen(v[kk], f);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], __fmul_rn(wk[kk], f[q]));
+                            for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], __fmul_rn(wk, f[q]));
+                        }
                     }
                 }
                 if (active) {
