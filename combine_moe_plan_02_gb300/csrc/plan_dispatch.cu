@@ -37,12 +37,17 @@ constexpr int kSeg = 512;       // bytes of a row segment copied by one warp
 #define MOE_PLAN_DISPATCH_FUSED_MAX 1024
 #endif
 constexpr int64_t kFusedMaxEntries = MOE_PLAN_DISPATCH_FUSED_MAX;
-// 256-thread CTAs when E <= 256: a quarter of the count table to clear and
-// scan (fp8 rows, H=6144 E=256 K=8, per call back to back in a graph: 6.54 ->
-// 4.57 us at 4..16 tokens, 8.60 -> 7.58 us at 128, 12.93 at 1024 either way;
-// two or four such CTAs per SM made 128 tokens slower, 9.2 us)
-#ifndef MOE_PD_NARROW
-#define MOE_PD_NARROW 1
+// CTAs of the smallest of 128, 256, 512 or 1024 threads that gives every
+// expert a thread (at least MOE_PD_MIN_THREADS): the per-warp count table
+// then has as many rows as the CTA has warps.  fp8 rows, H=6144 E=256 K=8,
+// per call back to back in a graph: 6.54 -> 4.57 us at 4..16 tokens with 256
+// threads instead of 1024, 8.60 -> 7.58 us at 128, 12.93 us at 1024 either
+// way; two or four such CTAs per SM made 128 tokens slower (9.2 us).  At
+// E=512, 512 threads: 4.5 against 6.3 us for 1024.  At E=64, 128 threads
+// gained 0.2 us at 4..16 tokens and lost 2 us at 128 (fewer warps rank and
+// copy), hence the floor of 256.
+#ifndef MOE_PD_MIN_THREADS
+#define MOE_PD_MIN_THREADS 256
 #endif
 
 __device__ uint32_t g_pd_error;  // kErrDispatchIndex
@@ -100,8 +105,7 @@ __device__ __forceinline__ int entry_key(const PDArgs &a, int64_t i, bool in_ran
     return (e >= 0 && e < a.E) ? e : -1;
 }
 
-// kT threads per CTA: 1024, or 256 when E <= 256 (a smaller count table to
-// clear and scan for the same ranks).
+// kT threads per CTA, at least E (one expert per thread in the totals).
 template <int kT>
 __global__ void __launch_bounds__(kT, 1) plan_dispatch_kernel(PDArgs a)
 {
@@ -159,11 +163,18 @@ __global__ void __launch_bounds__(kT, 1) plan_dispatch_kernel(PDArgs a)
     if (lane == 0 && invalid) atomicAdd(&s_inval, invalid);
     __syncthreads();
 
-    // totals and bucket offsets (thread e owns expert e)
+    // totals and bucket offsets (thread e owns expert e); the same walk
+    // turns expert e's warp counts into their exclusive prefixes over warps
     const int e = threadIdx.x;
     int32_t tot = 0;
-    if (e < a.E)
-        for (int w = 0; w < kW; ++w) tot += s_wc[w * wstride + e];
+    if (e < a.E) {
+#pragma unroll
+        for (int w = 0; w < kW; ++w) {
+            const int32_t c = s_wc[w * wstride + e];
+            s_wc[w * wstride + e] = tot;
+            tot += c;
+        }
+    }
     int32_t total;
     const int32_t offe = block_scan<kW>(tot, s_scan, total);
     if (e < a.E) {
@@ -178,16 +189,6 @@ __global__ void __launch_bounds__(kT, 1) plan_dispatch_kernel(PDArgs a)
         *a.n_invalid = s_inval;
     }
 
-    // per expert, exclusive scan over the warps (lane l holds warp l)
-    for (int k = warp; k < a.E; k += kW) {
-        const int32_t c = lane < kW ? s_wc[lane * wstride + k] : 0;
-        int32_t x = c;
-        for (int sh = 1; sh < kW; sh <<= 1) {
-            const int32_t y = __shfl_up_sync(0xffffffffu, x, sh);
-            if (lane >= sh) x += y;
-        }
-        if (lane < kW) s_wc[lane * wstride + k] = x - c;
-    }
     __syncthreads();
 
     // ranks
@@ -580,14 +581,18 @@ MOE_EXPORT int moe_plan_dispatch(const int32_t *topk_idx, const void *x, int64_t
     a.packed_rows = packed_rows;
 
     // one warp per (token, segment) unit, at most one CTA per SM
-    const bool narrow = MOE_PD_NARROW && E <= 256;
-    const int threads = narrow ? 256 : kThreads;
-    void (*fn)(PDArgs) = narrow ? plan_dispatch_kernel<256> : plan_dispatch_kernel<kThreads>;
+    int ti = 0;  // 128 << ti threads
+    while ((128 << ti) < E || (128 << ti) < MOE_PD_MIN_THREADS) ++ti;
+    static void (*const kFns[4])(PDArgs) = {plan_dispatch_kernel<128>, plan_dispatch_kernel<256>,
+                                           plan_dispatch_kernel<512>, plan_dispatch_kernel<1024>};
+    static_assert(kThreads == 1024, "the largest CTA gives every expert of E <= 1024 a thread");
+    const int threads = 128 << ti;
+    void (*fn)(PDArgs) = kFns[ti];
     const size_t smem =
         ((size_t)(threads / 32) * (E | 1) + (size_t)E + (size_t)n) * sizeof(int32_t);
-    static KernelCache caches[2];
+    static KernelCache caches[4];
     int per_sm = 0;
-    cudaError_t err = prepare_kernel(fn, smem, threads, caches[narrow], &per_sm);
+    cudaError_t err = prepare_kernel(fn, smem, threads, caches[ti], &per_sm);
     if (err != cudaSuccess || per_sm < 1) {
         set_cuda_error(err != cudaSuccess ? err : cudaErrorInvalidConfiguration);
         return MOE_ECUDA;
