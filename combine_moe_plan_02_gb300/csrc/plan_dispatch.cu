@@ -379,15 +379,24 @@ __global__ void __launch_bounds__(kThreads, 1) plan_dispatch_tiles_kernel(PDArgs
         a.off[a.E] = total;
         *a.n_invalid = s_inval;
     }
-    // per expert, exclusive scan over the warps of the range
-    for (int k = warp; k < a.E; k += kWarps) {
-        const int32_t c = s_wc[lane * wstride + k];
-        int32_t x = c;
-        for (int sh = 1; sh < 32; sh <<= 1) {
-            const int32_t y = __shfl_up_sync(0xffffffffu, x, sh);
-            if (lane >= sh) x += y;
+    // per expert, exclusive scan over the warps of the range: thread e walks
+    // expert e's column (16 counts loaded before any is rewritten; against
+    // one warp per expert scanning it with shuffles, back to back in a
+    // graph: 13.27 -> 12.44 us for 1024 fp8 tokens at E=256, 28.8 -> 26.1 us
+    // for 3000 tokens at E=1024 K=32)
+    if (e < a.E) {
+        int32_t run = 0;
+#pragma unroll
+        for (int w0 = 0; w0 < kWarps; w0 += 16) {
+            int32_t c[16];
+#pragma unroll
+            for (int w = 0; w < 16; ++w) c[w] = s_wc[(w0 + w) * wstride + e];
+#pragma unroll
+            for (int w = 0; w < 16; ++w) {
+                s_wc[(w0 + w) * wstride + e] = run;
+                run += c[w];
+            }
         }
-        s_wc[lane * wstride + k] = x - c;
     }
     __syncthreads();
 
