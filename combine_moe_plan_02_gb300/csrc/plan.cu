@@ -535,11 +535,19 @@ __global__ void __launch_bounds__(kThreads, 1) plan_rank_kernel(Key key, int nke
 
     // (b) global counts and counts of earlier tiles
     if (single) {
+        // totals; the same walk leaves each key's exclusive prefixes over
+        // the warps in place of its counts, which is step (d) (32 tokens at
+        // E=1024, per plan back to back in a graph: 5.5 -> 5.1 us)
         __syncthreads();
         for (int e = threadIdx.x; e < nkeys; e += kThreads) {
-            int32_t tot = 0;
-            for (int w = 0; w < kWarps; ++w) tot += s_wc[w * wstride + e];
-            s_tot[e] = tot;
+            int32_t run = 0;
+#pragma unroll 8
+            for (int w = 0; w < kWarps; ++w) {
+                const int32_t c = s_wc[w * wstride + e];
+                s_wc[w * wstride + e] = run;
+                run += c;
+            }
+            s_tot[e] = run;
         }
     } else if (g.mode == kModeFused) {
         // s_tot collects the entries from this tile on, s_bef those before
@@ -604,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1) plan_rank_kernel(Key key, int nke
     // key scanning the column with shuffles: 7.17 -> 7.0 us at S=4096 K=8
     // E=64, 10.57 -> 9.87 us for the Zipf batch (S=8192, E=256), 11.53 ->
     // 8.93 us at E=1024.
-    if (e < nkeys) {
+    if (!single && e < nkeys) {
         int32_t run = 0;
 #pragma unroll
         for (int w0 = 0; w0 < kWarps; w0 += 16) {

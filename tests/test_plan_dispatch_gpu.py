@@ -81,7 +81,7 @@ def test_fp8_rows_and_scales(S):
 @pytest.mark.parametrize("S,H,E,K", [(128, 7168, 64, 8), (3, 8, 1, 1), (32, 1032, 1024, 32),
                                      (33, 256, 1024, 31), (1000, 64, 7, 1), (17, 2056, 257, 5),
                                      (102, 264, 256, 10), (1, 64, 256, 8), (60, 520, 512, 16),
-                                     (90, 136, 128, 11), (7, 1040, 129, 3)])
+                                     (90, 136, 128, 11), (7, 1040, 129, 3), (40, 264, 513, 20)])
 def test_bf16_shapes(S, H, E, K):
     _check(workloads.make("moonep", seed=S + E, S=S, H=H, E=E, K=K))
 
