@@ -37,18 +37,15 @@ constexpr int kSeg = 512;       // bytes of a row segment copied by one warp
 #define MOE_PLAN_DISPATCH_FUSED_MAX 1024
 #endif
 constexpr int64_t kFusedMaxEntries = MOE_PLAN_DISPATCH_FUSED_MAX;
-// CTAs of the smallest of 128, 256, 512 or 1024 threads that gives every
-// expert a thread (at least MOE_PD_MIN_THREADS): the per-warp count table
-// then has as many rows as the CTA has warps.  fp8 rows, H=6144 E=256 K=8,
+// CTAs of the smallest of 256, 512 or 1024 threads that gives every expert
+// a thread: the per-warp count table then has as many rows as the CTA has
+// warps.  fp8 rows, H=6144 E=256 K=8,
 // per call back to back in a graph: 6.54 -> 4.57 us at 4..16 tokens with 256
 // threads instead of 1024, 8.60 -> 7.58 us at 128, 12.93 us at 1024 either
 // way; two or four such CTAs per SM made 128 tokens slower (9.2 us).  At
 // E=512, 512 threads: 4.5 against 6.3 us for 1024.  At E=64, 128 threads
 // gained 0.2 us at 4..16 tokens and lost 2 us at 128 (fewer warps rank and
 // copy), hence the floor of 256.
-#ifndef MOE_PD_MIN_THREADS
-#define MOE_PD_MIN_THREADS 256
-#endif
 
 __device__ uint32_t g_pd_error;  // kErrDispatchIndex
 
@@ -590,16 +587,16 @@ MOE_EXPORT int moe_plan_dispatch(const int32_t *topk_idx, const void *x, int64_t
     a.packed_rows = packed_rows;
 
     // one warp per (token, segment) unit, at most one CTA per SM
-    int ti = 0;  // 128 << ti threads
-    while ((128 << ti) < E || (128 << ti) < MOE_PD_MIN_THREADS) ++ti;
-    static void (*const kFns[4])(PDArgs) = {plan_dispatch_kernel<128>, plan_dispatch_kernel<256>,
-                                           plan_dispatch_kernel<512>, plan_dispatch_kernel<1024>};
+    int ti = 0;  // 256 << ti threads
+    while ((256 << ti) < E) ++ti;
+    static void (*const kFns[3])(PDArgs) = {plan_dispatch_kernel<256>, plan_dispatch_kernel<512>,
+                                           plan_dispatch_kernel<1024>};
     static_assert(kThreads == 1024, "the largest CTA gives every expert of E <= 1024 a thread");
-    const int threads = 128 << ti;
+    const int threads = 256 << ti;
     void (*fn)(PDArgs) = kFns[ti];
     const size_t smem =
         ((size_t)(threads / 32) * (E | 1) + (size_t)E + (size_t)n) * sizeof(int32_t);
-    static KernelCache caches[4];
+    static KernelCache caches[3];
     int per_sm = 0;
     cudaError_t err = prepare_kernel(fn, smem, threads, caches[ti], &per_sm);
     if (err != cudaSuccess || per_sm < 1) {
