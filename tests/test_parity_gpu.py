@@ -105,6 +105,39 @@ def test_dedup_edge_tokens(S):
     run_case(workloads.make("dedup", seed=1, S=S))
 
 
+@pytest.mark.parametrize("name,out_dt", [("dedup", "bf16"), ("dedup", "f32"), ("moonep", "f32"),
+                                         ("moonep", "bf16")])
+@pytest.mark.parametrize("H", [1032, 4096])
+def test_dedup_combine_dtypes(name, out_dt, H):
+    """The one-pass dedup combine for every (row, output) type pair, over
+    rows whose last 256-element warp-step is ragged (H=1032) or not: group
+    rows and outputs bitwise equal to the oracle's."""
+    import combine_moe_plan_02_gb300 as moe
+    wl = workloads.make(name, seed=5, S=300, H=H)
+    gs = 8
+    d = gpu_path.to_device(wl)
+    plan = moe.moe_plan(d["topk_idx"], wl.E)
+    gp = moe.moe_group_plan(d["topk_idx"], plan.tok_map, wl.E, gs)
+    _, packed = moe.moe_dispatch_dedup(d["x"], gp)
+    rmax = gp.grp_src.shape[0]
+    gtok = gpu_path.poisoned((rmax, H), torch.float32)
+    out = gpu_path.poisoned((wl.S, H), torch.float32 if out_dt == "f32" else torch.bfloat16)
+    moe.moe_combine_dedup(packed, d["topk_w"], gp, gtok=gtok, out=out, out_dtype=out.dtype)
+    torch.cuda.synchronize()
+    assert moe.moe_device_errors() == 0
+    p = oracle.plan(wl.topk_idx, wl.E)
+    ogp = oracle.group_plan(wl.topk_idx, p["tok_map"], wl.E, gs)
+    V = int(p["off"][-1])
+    _, opk = oracle.dispatch_dedup(wl.x, ogp["grp_src"], ogp["grp_tok_map"], wl.K, V)
+    in_dt = "f32" if wl.x.dtype == np.float32 else "bf16"
+    ref_gtok, ref_out = oracle.combine_dedup(opk, in_dt, wl.topk_w, ogp["grp_src"],
+                                             ogp["grp_tok_map"], ogp["gtok_map"], H, out_dt)
+    R = int(gp.goff[-1].item())
+    assert R == ogp["grp_src"].shape[0]
+    assert np.array_equal(gpu_path._np(gtok)[:R].view(np.uint32), ref_gtok[:R].view(np.uint32))
+    assert np.array_equal(gpu_path._np(out).view(np.uint8), ref_out.view(np.uint8))
+
+
 @pytest.mark.timeout(600)
 @pytest.mark.parametrize("S", workloads.FP8_SWEEP_TOKENS)
 def test_fp8_small_token_sweep(S):
