@@ -24,7 +24,7 @@ __all__ = [
     "moe_combine", "moe_combine_fold",
     "moe_combine_dedup", "moe_plan_workspace_size", "moe_group_plan_workspace_size",
     "moe_device_errors", "moe_plan_capacity", "Plan", "GroupPlan", "CapacityPlan", "MoeError",
-    "lib",
+    "MoeOp", "Routing", "lib",
 ]
 
 
@@ -367,3 +367,6 @@ def moe_device_errors() -> int:
     v = ctypes.c_uint32(0)
     _abi.check("moe_device_errors", lib().moe_device_errors(ctypes.byref(v)))
     return int(v.value)
+
+
+from .op import MoeOp, Routing  # noqa: E402  (the op interface over the calls above)
