@@ -1,4 +1,5 @@
-"""The pages' op interface over the library's stateless calls.
+"""The op interface of ROCm/mori's dispatch/combine over the library's
+stateless calls.
 
 ROCm/mori "Draft: cco + flydsl dispatch/combine #448" drives the path
 through one op object (the op notes and the routing-handle note):
@@ -27,7 +28,7 @@ Modes (fixed when the op is made):
             moe_group_plan, moe_dispatch_dedup, moe_combine_dedup)
 
 combine: weighted (sum_k w[s,k] * y[row]) or unweighted (the sum of the
-copies, the pages' identity round trip), both in f32 in increasing k;
+copies: the op notes' identity round trip), both in f32 in increasing k;
 combined_wts[s,i] is the sum of topk_w[s,i] over the token's valid copies
 (the weight fold).  In dedup mode the weights are applied inside each group
 row and the group rows are summed unweighted; the fold there takes a second
