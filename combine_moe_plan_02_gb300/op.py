@@ -40,9 +40,9 @@ from typing import NamedTuple, Optional
 
 import torch
 
-from . import (CapacityPlan, GroupPlan, Plan, moe_combine_dedup, moe_combine_fold,
-               moe_dispatch, moe_dispatch_dedup, moe_dispatch_quant_fp8, moe_group_plan,
-               moe_plan, moe_plan_capacity, moe_plan_dispatch)
+from . import (GroupPlan, moe_combine_dedup, moe_combine_fold, moe_dispatch,
+               moe_dispatch_dedup, moe_dispatch_quant_fp8, moe_group_plan, moe_plan,
+               moe_plan_capacity, moe_plan_dispatch)
 
 __all__ = ["MoeOp", "Routing"]
 

@@ -1,9 +1,8 @@
-"""MoeOp, the op interface of ROCm/mori's dispatch/combine (out, total_recv,
-routing = op.dispatch(x,
-topk_w, topk_idx); combined, combined_wts = op.combine(y, routing); ROCm/mori
-"Draft: cco + flydsl dispatch/combine #448", op notes), in every mode,
-against the CPU oracle: dispatch outputs, total_recv, the combine and the
-weight fold, bitwise."""
+"""MoeOp, the op interface of ROCm/mori's dispatch/combine (ROCm/mori "Draft:
+cco + flydsl dispatch/combine #448", op notes: out, total_recv, routing =
+op.dispatch(x, topk_w, topk_idx); combined, combined_wts = op.combine(y,
+routing)), in every mode, against the CPU oracle: dispatch outputs,
+total_recv, the combine and the weight fold, bitwise."""
 import numpy as np
 import pytest
 
