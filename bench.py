@@ -573,6 +573,77 @@ def _small_token_sweep(moe, torch, dev, stream, reps, res):
 
 
 # ---------------------------------------------------------------------------
+# the step under contention (MoonEP "Drop cooperative launch from the
+# CTA-independent local kernels": the local kernels timed alone and against a
+# saturating GEMM stream, 100 launches)
+# ---------------------------------------------------------------------------
+
+def contended_step(torch, moe, dev, stream, idx, x, w, y, plan, packed, out, ws, E, n=100):
+    """µs per call of the step's two calls, alone and while bf16 GEMMs
+    (8192 x 8192 x 8192, torch.matmul) keep the GPU busy on another stream.
+    The library's CTAs are independent (no cooperative launch, no grid-wide
+    wait), so they share the SMs with the GEMM's instead of waiting for the
+    whole GPU.  No L2 flush between steps in either run."""
+    side = torch.cuda.Stream(dev)
+    a = torch.randn(8192, 8192, device=dev).to(torch.bfloat16)
+    b = torch.randn(8192, 8192, device=dev).to(torch.bfloat16)
+    c = torch.empty(8192, 8192, device=dev, dtype=torch.bfloat16)
+
+    def steps(evs):
+        for e in evs:
+            e[0].record(stream)
+            moe.moe_plan_dispatch(idx, x, E, out=plan, packed_x=packed, workspace=ws,
+                                  stream=stream)
+            e[1].record(stream)
+            moe.moe_combine(y, w, plan.tok_map, out=out, stream=stream)
+            e[2].record(stream)
+
+    def mk():
+        return [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        torch.matmul(a, b, out=c)
+    g0.record()
+    for _ in range(5):
+        torch.matmul(a, b, out=c)
+    g1.record()
+    torch.cuda.synchronize()
+    one_gemm_ms = g0.elapsed_time(g1) / 5
+    iso = mk()
+    steps(iso)
+    torch.cuda.synchronize()
+    iso_ms = iso[0][0].elapsed_time(iso[-1][2])
+    # GEMMs enqueued first, enough to outlast the steps even when the steps
+    # run several times slower than alone
+    n_gemm = int(8 * iso_ms / one_gemm_ms) + 1
+    g0.record(side)
+    with torch.cuda.stream(side):
+        for _ in range(n_gemm):
+            torch.matmul(a, b, out=c)
+    g1.record(side)
+    con = mk()
+    steps(con)
+    torch.cuda.synchronize()
+    covered = g0.elapsed_time(g1) > g0.elapsed_time(con[-1][2])
+    gemm_ms = g0.elapsed_time(g1)
+
+    def m(evs, i, j):
+        return round(1e3 * statistics.mean(e[i].elapsed_time(e[j]) for e in evs), 2)
+
+    res = {"what": f"moe_plan_dispatch and moe_combine at the headline shape, {n} steps, "
+                   f"alone and while {n_gemm} bf16 8192^3 GEMMs run on another stream",
+           "alone_us": {"plan_dispatch": m(iso, 0, 1), "combine": m(iso, 1, 2)},
+           "contended_us": {"plan_dispatch": m(con, 0, 1), "combine": m(con, 1, 2)},
+           "gemm_stream_busy_throughout": bool(covered),
+           "gemm_tflops_alone": round(2 * 8192 ** 3 / (one_gemm_ms * 1e-3) / 1e12, 1),
+           "gemm_tflops_during": round(n_gemm * 2 * 8192 ** 3 / (gemm_ms * 1e-3) / 1e12, 1)}
+    del a, b, c
+    return res
+
+
+# ---------------------------------------------------------------------------
 # GPU leg
 # ---------------------------------------------------------------------------
 
@@ -981,6 +1052,9 @@ def run_ours(args):
         line["small_tokens"] = small_token_latency(dev)
     if rank == 0 and not args.no_other_workloads:
         line["other_workloads"] = other_workloads(torch, moe, dev, stream, flush_l2, peak)
+        if not args.no_contended:
+            line["contended"] = contended_step(torch, moe, dev, stream, idx, x, w, y, plan,
+                                               packed, out, ws, E)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:
@@ -1003,6 +1077,9 @@ def main(argv=None):
                     help="skip the timed CPU oracle leg (profiling runs)")
     ap.add_argument("--no-small-tokens", action="store_true",
                     help="skip the small-token latency sweep (profiling runs)")
+    ap.add_argument("--no-contended", action="store_true",
+                    help="skip the step timed against a concurrent GEMM stream (it runs "
+                         "with the other workloads)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
