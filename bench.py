@@ -589,14 +589,13 @@ def contended_step(torch, moe, dev, stream, idx, x, w, y, plan, packed, out, ws,
     b = torch.randn(8192, 8192, device=dev).to(torch.bfloat16)
     c = torch.empty(8192, 8192, device=dev, dtype=torch.bfloat16)
 
-    def steps(evs):
+    def steps(evs, st=stream):
         for e in evs:
-            e[0].record(stream)
-            moe.moe_plan_dispatch(idx, x, E, out=plan, packed_x=packed, workspace=ws,
-                                  stream=stream)
-            e[1].record(stream)
-            moe.moe_combine(y, w, plan.tok_map, out=out, stream=stream)
-            e[2].record(stream)
+            e[0].record(st)
+            moe.moe_plan_dispatch(idx, x, E, out=plan, packed_x=packed, workspace=ws, stream=st)
+            e[1].record(st)
+            moe.moe_combine(y, w, plan.tok_map, out=out, stream=st)
+            e[2].record(st)
 
     def mk():
         return [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
@@ -628,6 +627,22 @@ def contended_step(torch, moe, dev, stream, idx, x, w, y, plan, packed, out, ws,
     torch.cuda.synchronize()
     covered = g0.elapsed_time(g1) > g0.elapsed_time(con[-1][2])
     gemm_ms = g0.elapsed_time(g1)
+    # the same with the step on a stream of the highest priority: its CTAs
+    # go first whenever an SM frees up
+    hp = torch.cuda.Stream(dev, priority=torch.cuda.Stream.priority_range()[1]
+                           if hasattr(torch.cuda.Stream, "priority_range") else -1)
+    h0 = torch.cuda.Event(enable_timing=True)
+    h1 = torch.cuda.Event(enable_timing=True)
+    h0.record(side)
+    with torch.cuda.stream(side):
+        for _ in range(n_gemm):
+            torch.matmul(a, b, out=c)
+    h1.record(side)
+    con_hp = mk()
+    steps(con_hp, hp)
+    torch.cuda.synchronize()
+    covered_hp = h0.elapsed_time(h1) > h0.elapsed_time(con_hp[-1][2])
+    gemm_hp_ms = h0.elapsed_time(h1)
 
     def m(evs, i, j):
         return round(1e3 * statistics.mean(e[i].elapsed_time(e[j]) for e in evs), 2)
@@ -638,7 +653,12 @@ def contended_step(torch, moe, dev, stream, idx, x, w, y, plan, packed, out, ws,
            "contended_us": {"plan_dispatch": m(con, 0, 1), "combine": m(con, 1, 2)},
            "gemm_stream_busy_throughout": bool(covered),
            "gemm_tflops_alone": round(2 * 8192 ** 3 / (one_gemm_ms * 1e-3) / 1e12, 1),
-           "gemm_tflops_during": round(n_gemm * 2 * 8192 ** 3 / (gemm_ms * 1e-3) / 1e12, 1)}
+           "gemm_tflops_during": round(n_gemm * 2 * 8192 ** 3 / (gemm_ms * 1e-3) / 1e12, 1),
+           "high_priority_stream": {
+               "contended_us": {"plan_dispatch": m(con_hp, 0, 1), "combine": m(con_hp, 1, 2)},
+               "gemm_stream_busy_throughout": bool(covered_hp),
+               "gemm_tflops_during": round(n_gemm * 2 * 8192 ** 3 / (gemm_hp_ms * 1e-3) / 1e12,
+                                           1)}}
     del a, b, c
     return res
 
