@@ -42,6 +42,10 @@
  *     [0, E) is counted in *n_invalid and its entries are marked -1.
  *   - S = 0 is valid: moe_plan still writes zero counts/offsets; the other
  *     calls enqueue nothing.
+ *   - No kernel waits for other CTAs or needs the whole GPU (no cooperative
+ *     launch; MoonEP page above), so the calls share the GPU with work on
+ *     other streams.  Beside a compute-bound kernel (an expert GEMM), a
+ *     stream of high priority lets their CTAs take SMs first as they free up.
  */
 #ifndef MOE_PLAN_H
 #define MOE_PLAN_H
