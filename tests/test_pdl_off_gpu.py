@@ -28,7 +28,8 @@ pytestmark = [pytest.mark.gpu,
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 # the full-size workloads, the plan modes (one tile, one launch, two kernels,
-# static scratch), the one-launch plan + dispatch, graphs, capacity and dedup
+# static scratch), the one-launch plan + dispatch, graphs, capacity, dedup and
+# batches on several streams at once
 PDL_OFF_CASES = [
     "tests/test_parity_gpu.py::test_moonep_full_size",
     "tests/test_parity_gpu.py::test_zipf_full_size",
@@ -42,6 +43,8 @@ PDL_OFF_CASES = [
     "tests/test_capacity_gpu.py::test_dedup_over_capacity_plan",
     "tests/test_combine_large_gpu.py",
     "tests/test_zz_no_alloc.py",
+    "tests/test_graph_gpu.py",
+    "tests/test_streams_gpu.py",
     "tests/test_pdl_off_gpu.py::test_loaded_library_is_the_requested_build",
 ]
 
