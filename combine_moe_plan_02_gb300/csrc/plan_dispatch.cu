@@ -12,10 +12,11 @@
 // fused.  Below the crossover the flat entry list holds at most
 // kFusedMaxEntries entries, few enough that every CTA of the launch ranks all
 // of them itself in shared memory -- the same stable (token, k) ranks as
-// moe_plan: per-warp counts by __match_any_sync, totals, an exclusive scan
-// over experts, a scan over warps per expert, then rank = expert offset +
-// warp base + running count + popc(peers below the lane).  CTA 0 also writes
-// the plan outputs.  Then every warp of the grid copies 512-byte segments of
+// moe_plan: per-warp counts by __match_any_sync, then thread e walks expert
+// e's warp counts (its total, and the exclusive prefix over warps left in
+// place), an exclusive scan over experts, then rank = expert offset + warp
+// base + running count + popc(peers below the lane).  CTA 0 also writes the
+// plan outputs.  Then every warp of the grid copies 512-byte segments of
 // token rows (32 lanes x 16 bytes) to the token's destinations, read from
 // the CTA's own copy of the map.  No CTA waits for another CTA.
 //
