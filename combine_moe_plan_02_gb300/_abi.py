@@ -43,6 +43,7 @@ SIGNATURES = {
                                 P, SZ, P]),
     "moe_device_errors": (I32, [P]),
     "moe_selftest_wait_timeout": (I32, [I64, P]),
+    "moe_selftest_convert": (I32, [ctypes.c_uint32, I64, P, P, P]),
 }
 
 _lib = None

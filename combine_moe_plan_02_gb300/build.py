@@ -16,7 +16,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_gb300.so")
-SOURCES = ["plan.cu", "plan_dispatch.cu", "dispatch.cu", "combine.cu", "status.cu"]
+SOURCES = ["plan.cu", "plan_dispatch.cu", "dispatch.cu", "combine.cu", "status.cu", "selftest.cu"]
 HEADERS = ["common.cuh", os.path.join("..", "..", "include", "moe_plan.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

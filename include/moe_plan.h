@@ -106,6 +106,24 @@ int moe_device_errors(uint32_t *flags);
  * CUDA context stays usable.  Asynchronous on `stream`. */
 int moe_selftest_wait_timeout(int64_t limit_ns, moe_stream_t stream);
 
+/* Self-test of the number-format conversions the kernels use [mori #448:
+ * Fp8BlockwiseQuant notes (the fp8 cast of each scaled element) and the
+ * accumulator note (f32 sums stored back as bf16)]: for i in [0, count) the
+ * binary32 value with bit pattern first + i is converted
+ *   - to E4M3 exactly as the quantising dispatch casts its quotients (OCP
+ *     OFP8 v1.0 E4M3, round to nearest even, saturated to +-448, NaN to a
+ *     NaN code) into e4m3_out[i], when e4m3_out is not NULL;
+ *   - to bfloat16 exactly as the combines store their f32 sums (round to
+ *     nearest even) into bf16_out[i], when bf16_out is not NULL.
+ * first and count: multiples of 4, first + count <= 2^32 (the whole
+ * binary32 range in one call needs 4 GiB of e4m3_out and 8 GiB of bf16_out).
+ * e4m3_out [count] u8, bf16_out [count] u16: DEVICE pointers, 16-byte
+ * aligned, owned by the caller; at least one of them set.
+ * Errors: MOE_EINVAL (ranges, both outputs NULL), MOE_EALIGN; asynchronous on
+ * `stream`. */
+int moe_selftest_convert(uint32_t first, int64_t count, uint8_t *e4m3_out, uint16_t *bf16_out,
+                         moe_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Plan  [mori #448: StdMoE note (packed_cnt, packed_src, i64 slot map with
  * -1) and routing-handle note (local_expert_count)].

@@ -200,3 +200,15 @@ def test_capacity_plan_validation(L):
     assert c(cap=1 << 30, E=8) == EINVAL      # E * capacity >= 2^31
     assert c(nd=None) == EINVAL
     assert c(S=-1) == EINVAL
+
+
+def test_selftest_convert_rejects_bad_ranges(L):
+    f = L.moe_selftest_convert
+    assert f(1, 4, FAKE, None, None) == EINVAL             # first not a multiple of 4
+    assert f(0, 6, FAKE, None, None) == EINVAL             # count not a multiple of 4
+    assert f(0, -4, FAKE, None, None) == EINVAL
+    assert f(0xfffffffc, 8, FAKE, None, None) == EINVAL    # past 2^32
+    assert f(0, 4, None, None, None) == EINVAL             # no output
+    assert f(0, 4, MIS, None, None) == EALIGN
+    assert f(0, 4, None, MIS, None) == EALIGN
+    assert f(0, 0, FAKE, FAKE, None) == OK                 # nothing to do, nothing enqueued
