@@ -161,6 +161,8 @@ def test_fp8_small_token_sweep(S):
     (777, 24, 1024, 32),   # E = 1024 (largest), K = 32
     (5000, 256, 37, 5),    # E not a power of two
     (40000, 16, 256, 8),   # many tiles (320000 entries)
+    (524288, 8, 1024, 8),  # 4.2M entries: two-kernel plan over 128 tiles, E = 1024
+    (131072, 8, 512, 32),  # K = 32 at 4.2M entries
 ])
 def test_shapes(S, H, E, K):
     run_case(workloads.make("moonep", seed=S + H, S=S, H=H, E=E, K=K))
