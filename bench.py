@@ -446,6 +446,14 @@ def run_reference(args):
 # 4..32 tokens; here on one GPU with fp8 rows and per-128 scales)
 # ---------------------------------------------------------------------------
 
+def _trimmed_mean(xs, cut: float = 0.1):
+    """Mean of the values left after dropping the lowest and highest `cut`
+    fraction."""
+    v = sorted(xs)
+    k = int(len(v) * cut)
+    return statistics.mean(v[k:len(v) - k] if len(v) > 2 * k else v)
+
+
 def small_token_latency(dev, reps: int = 50):
     """µs per plan + dispatch (fp8 rows + f32 scales) + combine (bf16) call
     sequence at small token counts, eager and replayed from a CUDA graph."""
@@ -556,9 +564,11 @@ def _small_token_sweep(moe, torch, dev, stream, reps, res):
             gf.replay()
             b.record(stream)
         torch.cuda.synchronize()
-        # means: CUDA event timestamps come in steps of about 2 us on this
-        # part, so medians of short launches snap to those steps
-        med = lambda xs_: round(1e3 * statistics.mean(xs_), 2)
+        # means of the middle 80 %: CUDA event timestamps come in steps of
+        # about 2 us on this part, so medians of short launches snap to those
+        # steps, and a plain mean takes in the odd host-side stall of an
+        # eager call (one 1 ms outlier moves a mean of 50 by 20 us)
+        med = lambda xs_: round(1e3 * _trimmed_mean(xs_), 2)
         res["fused_eager_us"].append(med([a.elapsed_time(b) for a, b in fs_ev]))
         res["plan_dispatch_us"].append(med([e[0].elapsed_time(e[1]) for e in f_ev]))
         res["fused_graph_us"].append(med([a.elapsed_time(b) for a, b in gf_ev]))
