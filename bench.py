@@ -741,9 +741,13 @@ def other_workloads(torch, moe, dev, stream, flush_l2, peak):
     packed = torch.empty(S * K, H, dtype=torch.float32, device=dev)
     gtok = torch.empty(gp.max_rows, H, dtype=torch.float32, device=dev)
     out = torch.empty(S, H, dtype=torch.float32, device=dev)
+    # the group plan's tile histograms: allocated once, as a caller's loop would
+    gws = torch.empty(max(moe.moe_group_plan_workspace_size(S, K, E, gs), 256), dtype=torch.uint8,
+                      device=dev)
     t = _timed_calls(torch, stream, flush_l2, {
         "plan": lambda: moe.moe_plan(idx, E, out=plan, stream=stream),
-        "group_plan": lambda: moe.moe_group_plan(idx, plan.tok_map, E, gs, out=gp, stream=stream),
+        "group_plan": lambda: moe.moe_group_plan(idx, plan.tok_map, E, gs, out=gp, workspace=gws,
+                                                 stream=stream),
         "dispatch_dedup": lambda: moe.moe_dispatch_dedup(x, gp, grp_x=grp_x, packed_x=packed,
                                                          stream=stream),
         "combine_dedup": lambda: moe.moe_combine_dedup(packed, w, gp, gtok=gtok, out=out,
